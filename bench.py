@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Throughput of fbob_bob (exact attention backward-over-backward) on GB300.
+
+One step = one fbob_bob call (every pass of the BoB path) over one batch of
+the synthetic workload, with the forward's O and LSE precomputed (the call's
+inputs).  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the
+                                         # host cores on a bounded sample
+
+For N > 1 (launched by torchrun) every rank runs its own instance of the
+workload (independent (batch, head) units, no data-path collective): weak
+scaling; the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fbob_bob TFLOP/s & ms/call, bf16 causal d=128, N=16K–262K; % of BF16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "bf16_causal_b2h16_n16384_d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+# Algorithmic N x N x d products per kernel of each kernel family (one
+# product = 2*N^2*d FLOP per (batch, head), halved when causal).
+KERNELS = {
+    1: [("bob_row_pass", 5), ("bob_col_pass", 10), ("gradq_convert", 0)],
+    0: [("simt_row_pass1", 5), ("simt_col_pass", 8), ("simt_row_pass_gradq", 7)],
+}
+
+
+# ------------------------------------------------------------ host logic ---
+
+def flops_bob(w, products: int = 15) -> float:
+    """FLOP of BoB: products * 2 * B*H*N^2*d, halved for a causal mask
+    (30*B*H*N^2*d for the 15 products of the two-pass schedule)."""
+    f = 2.0 * products * w.B * w.H * float(w.N) ** 2 * w.d
+    return f * (0.5 if w.causal else 1.0)
+
+
+def causal_pairs(rows, causal: bool, n: int) -> int:
+    return int(sum((r + 1) if causal else n for r in rows))
+
+
+def shard_units(n_units: int, rank: int, world: int) -> range:
+    """Contiguous share of n_units independent (batch, head) units for a rank."""
+    per, rem = divmod(n_units, world)
+    start = rank * per + min(rank, rem)
+    return range(start, start + per + (1 if rank < rem else 0))
+
+
+def reduce_max(value: float, dist) -> float:
+    """Max of a scalar over ranks (timing only; no data-path collective)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    return dict(FALLBACK_PEAKS)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_second_order_two_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or
+    None if there is none or the kernel sources changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    entry = rec.get(workload, {}).get(kernel)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(device_index)],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, mx, power, reasons = [], [], [], set()
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.file.name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "samples": len(sm), "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons)}
+
+
+def smi_index(torch) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    cur = torch.cuda.current_device()
+    ids = [x.strip() for x in vis.split(",") if x.strip()]
+    if ids and all(x.isdigit() for x in ids) and cur < len(ids):
+        return int(ids[cur])
+    return cur
+
+
+# ------------------------------------------------------------- CPU oracle ---
+
+def oracle_sample(w, ins, budget_s: float, rows_per_block: int = 128):
+    """Times the fp64 oracle on query-row blocks of head (0, 0), last rows
+    first, until `budget_s` seconds of work are done.  Returns (TFLOP/s by
+    the BoB formula's per-pair count, description)."""
+    import numpy as np
+
+    import oracle
+    x = {k: v[0, 0].double().numpy() for k, v in ins.items()}
+    args = (x["q"], x["k"], x["v"], x["do"], x["gq"], x["gk"], x["gv"], w.causal, w.scale)
+    done_rows, elapsed, blocks = [], 0.0, 0
+    end = w.N
+    while elapsed < budget_s and end > 0:
+        rows = np.arange(max(0, end - rows_per_block), end)
+        t0 = time.perf_counter()
+        oracle.bob_rows(*args, rows, row_block=rows_per_block)
+        elapsed += time.perf_counter() - t0
+        done_rows.extend(rows.tolist())
+        end -= rows_per_block
+        blocks += 1
+    pairs = causal_pairs(done_rows, w.causal, w.N)
+    flop = 30.0 * w.d * pairs
+    desc = (f"fp64 oracle, head (0,0) of {w.name}: {len(done_rows)} query rows "
+            f"(last rows first, {blocks} blocks of {rows_per_block}), "
+            f"{pairs} visible (query,key) pairs, {elapsed:.1f} s")
+    return flop / elapsed / 1e12, desc, elapsed
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------- arms ---
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    import torch
+    from exact_second_order_two_gb300.synthetic import make_inputs
+    ins = make_inputs(w.with_(B=1, H=1), seed=args.seed)
+    per_step = []
+    for s in range(args.warmup + args.steps):
+        tput, desc, el = oracle_sample(w, ins, budget_s=args.ref_step_seconds)
+        if s >= args.warmup:
+            per_step.append((tput, el, desc))
+    value = statistics.median(t for t, _, _ in per_step)
+    ms = statistics.median(e for _, e, _ in per_step) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(),
+                         "kind": "oracle", "sample": per_step[-1][2]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    del torch
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w) -> dict:
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+            "dtype": w.dtype, "causal": w.causal, "scale": "1/sqrt(d)",
+            "inputs": f"Q,K ~ N(0,{w.qk_std}^2), V ~ N(0,{w.v_std}^2), "
+                      f"dO,gQ,gK,gV ~ N(0,{w.cot_std}^2), seeded",
+            "flop_formula": "30*B*H*N^2*d" + ("/2 (causal)" if w.causal else ""),
+            "l2": "inputs larger than L2: each [B,H,N,d] tensor is "
+                  f"{w.B * w.H * w.N * w.d * (2 if w.dtype == 'bf16' else 4) / 2**20:.0f} MiB"}
+
+
+def run_ours(args, w, rank, world, dist):
+    import torch
+
+    import exact_second_order_two_gb300 as fbob
+    from exact_second_order_two_gb300.synthetic import make_inputs
+
+    fbob.build_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    host = make_inputs(w, seed=args.seed + rank)
+    ins = {k: v.to(dev) for k, v in host.items()}
+    q, k, v, do, gq, gk, gv = (ins[n] for n in ("q", "k", "v", "do", "gq", "gk", "gv"))
+    o, lse = fbob.forward(q, k, v, w.causal, w.scale)
+    shp = fbob.shape_of(q, w.causal, w.scale)
+    ws = fbob.alloc_workspace(fbob.OP_BOB, shp, dev)
+    outs = tuple(torch.empty_like(q) for _ in range(4))
+    kpath = fbob.path(fbob.OP_BOB, shp)
+    kernels = KERNELS[kpath]
+
+    def call():
+        fbob.bob(q, k, v, o, lse, do, gq, gk, gv, w.causal, w.scale, out=outs, workspace=ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    if fbob.status(ws) != 0:
+        raise RuntimeError(f"device status {fbob.status(ws)} after warm-up")
+    n_events = len(kernels) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)]
+           for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if dist is not None and dist.is_initialized():
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(smi_index(torch)) if rank == 0 else None
+    launches = 0
+    start.record()
+    for s in range(args.steps):
+        fbob.set_profile_events(evs[s])
+        call()
+        launches += fbob.last_launch_count()
+    stop.record()
+    torch.cuda.synchronize()
+    fbob.set_profile_events([])
+    clocks = sampler.stop() if sampler else None
+    if dist is not None and dist.is_initialized():
+        dist.barrier()
+    if fbob.status(ws) != 0:
+        raise RuntimeError(f"device status {fbob.status(ws)} in timed region")
+    ms_local = start.elapsed_time(stop) / args.steps
+    ms = reduce_max(ms_local, dist)
+    flop = flops_bob(w)
+    value = world * flop / (ms * 1e-3) / 1e12
+
+    # per-kernel durations over the timed region
+    per_kernel = []
+    for m, (name, products) in enumerate(kernels):
+        t = statistics.mean(evs[s][m].elapsed_time(evs[s][m + 1]) for s in range(args.steps))
+        per_kernel.append((name, products, t))
+    dom = max(per_kernel, key=lambda x: x[2])
+    peaks = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    achieved = flops_bob(w, dom[1]) / (dom[2] * 1e-3) / 1e12 if dom[1] else 0.0
+
+    # end to end through the public API with pinned host buffers
+    e2e = run_e2e(args, w, host, o, lse, outs, ws, call_api=fbob.bob, dev=dev)
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tput, desc, _ = oracle_sample(w, host, budget_s=args.cpu_seconds)
+        cpu = {"value": tput, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": desc}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": workload_config(w),
+        "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+        "kernel_family": "tcgen05" if kpath == 1 else "simt",
+        "kernels_ms": {n: t for n, _, t in per_kernel},
+        "roofline": {"bound": "tensor", "kernel": dom[0], "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_kind": f"bf16 dense sustained ({peaks.get('source')})",
+                     "frac_of_burst": achieved / peaks["bf16_tflops"],
+                     "traffic": recorded_traffic(dom[0], w.name)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, host, o, lse, outs, ws, call_api, dev):
+    """Same metric through the public API: every step copies the inputs from
+    pinned host memory and reads the four results back."""
+    import torch
+    names = ("q", "k", "v", "do", "gq", "gk", "gv")
+    h_in = {n: host[n].pin_memory() for n in names}
+    h_in["o"] = o.cpu().pin_memory()
+    h_in["lse"] = lse.cpu().pin_memory()
+    d_in = {n: torch.empty_like(h_in[n], device=dev) for n in h_in}
+    h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def step():
+        for n in h_in:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        res = call_api(d_in["q"], d_in["k"], d_in["v"], d_in["o"], d_in["lse"], d_in["do"],
+                       d_in["gq"], d_in["gk"], d_in["gv"], w.causal, w.scale, out=outs,
+                       workspace=ws)
+        for h, d in zip(h_out, res):
+            h.copy_(d, non_blocking=True)
+
+    steps = max(2, min(args.steps, args.e2e_steps))
+    step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": flops_bob(w) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=6.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from exact_second_order_two_gb300.synthetic import WORKLOADS
+    w = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, w, rank, world)
+        else:
+            run_ours(args, w, rank, world, dist)
+    finally:
+        if dist is not None and dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

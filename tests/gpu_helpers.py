@@ -1,0 +1,110 @@
+"""Helpers for the GPU tests: run the CUDA path through the C ABI, run the
+oracle on the same (dtype-rounded) inputs, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import exact_second_order_two_gb300 as fbob
+from exact_second_order_two_gb300.synthetic import Workload, make_inputs
+
+import oracle
+
+BF16_TOL = 2e-2   # max|err| / max|ref| for bf16 inputs
+FP32_TOL = 1e-4   # max|err| / max|ref| for fp32 inputs
+
+
+def tol_for(w: Workload) -> float:
+    return FP32_TOL if w.dtype == "fp32" else BF16_TOL
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def rel_err(got, ref, floor: float = 1e-3) -> float:
+    """max|got - ref| / max|ref|.  Outputs that are identically zero in exact
+    arithmetic (e.g. dQ at N = 1) leave only rounding noise of cancelled
+    O(1) terms; the denominator is floored at ``floor`` (far below the O(0.1)
+    magnitude of every output on these inputs) so such cases compare
+    absolute error against that floor instead of dividing by zero."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    denom = max(float(np.max(np.abs(ref))), floor)
+    return float(np.max(np.abs(got - ref)) / denom)
+
+
+def gpu_pipeline(ins: dict, w: Workload, device="cuda"):
+    """forward -> backward -> BoB on the GPU, all through the C ABI."""
+    d = {k: v.to(device) for k, v in ins.items()}
+    o, lse = fbob.forward(d["q"], d["k"], d["v"], w.causal, w.scale)
+    dq, dk, dv = fbob.backward(d["q"], d["k"], d["v"], o, lse, d["do"],
+                               w.causal, w.scale)
+    grads = fbob.bob(d["q"], d["k"], d["v"], o, lse, d["do"], d["gq"], d["gk"],
+                     d["gv"], w.causal, w.scale)
+    torch.cuda.synchronize()
+    return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv, gradq=grads[0],
+                gradk=grads[1], gradv=grads[2], graddo=grads[3], dev=d)
+
+
+def oracle_full(ins: dict, w: Workload):
+    """Full fp64 oracle on the dtype-rounded inputs, per (b, h)."""
+    x = {k: to64(v) for k, v in ins.items()}
+    o, lse = oracle.forward_batched(x["q"], x["k"], x["v"], w.causal, w.scale)
+    dq, dk, dv = oracle.backward_batched(x["q"], x["k"], x["v"], x["do"],
+                                         w.causal, w.scale)
+    gq, gk, gv, gdo = oracle.bob_batched(x["q"], x["k"], x["v"], x["do"], x["gq"],
+                                         x["gk"], x["gv"], w.causal, w.scale)
+    return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv, gradq=gq, gradk=gk, gradv=gv,
+                graddo=gdo)
+
+
+def invariant_residuals(gpu: dict):
+    """Normalised residuals of the exact BoB invariants on GPU outputs.
+
+    Each identity <a,b> = c is reported as |<a,b> - c| / sqrt(sum (a*b)^2 +
+    ...): the size a rounding error of relative size eps produces is ~eps,
+    while a wrong term produces ~1.
+      I1  <graddO, dO> = L
+      I2  <gradV, V>  = <gQ,dQ> + <gK,dK>
+      I3  <gradQ, Q> - <gradK, K> = <gK,dK> - <gQ,dQ>
+      I4  sum_j gradK_j = 0 and sum_j gradV_j = 0 per (b, h)
+    with L = <gQ,dQ> + <gK,dK> + <gV,dV> from the GPU's first backward.
+    """
+    f = lambda t: t.double()  # noqa: E731
+    dv_ = gpu["dev"]
+
+    def ip(a, b):
+        prod = f(a) * f(b)
+        return prod.sum().item(), torch.sqrt((prod * prod).sum()).item()
+
+    gq_dq, s1 = ip(dv_["gq"], gpu["dq"])
+    gk_dk, s2 = ip(dv_["gk"], gpu["dk"])
+    gv_dv, s3 = ip(dv_["gv"], gpu["dv"])
+    L = gq_dq + gk_dk + gv_dv
+    a1, t1 = ip(gpu["graddo"], dv_["do"])
+    a2, t2 = ip(gpu["gradv"], dv_["v"])
+    a3q, t3q = ip(gpu["gradq"], dv_["q"])
+    a3k, t3k = ip(gpu["gradk"], dv_["k"])
+    res = {
+        "I1": abs(a1 - L) / (t1 + s1 + s2 + s3),
+        "I2": abs(a2 - (gq_dq + gk_dk)) / (t2 + s1 + s2),
+        "I3": abs((a3q - a3k) - (gk_dk - gq_dq)) / (t3q + t3k + s1 + s2),
+    }
+    for name in ("gradk", "gradv"):
+        g = f(gpu[name])
+        col_sum = g.sum(dim=2)                              # [B, H, d]
+        col_scale = torch.sqrt((g * g).sum(dim=2))
+        res["I4_" + name] = (col_sum.abs() / col_scale.clamp_min(1e-30)).max().item()
+    return res
+
+
+def sample_rows(N: int, count: int, seed: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    rows = set([0, N - 1, N // 2])
+    rows |= set(rng.integers(0, N, size=count).tolist())
+    return np.array(sorted(rows))
+
+
+def make(w: Workload, seed: int = 0):
+    return make_inputs(w, seed=seed, device="cpu")

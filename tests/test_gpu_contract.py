@@ -1,0 +1,97 @@
+"""GPU checks of the C ABI contract: outputs fully overwritten and nothing
+written outside them (canaries, in place of a memory sanitizer), error
+codes, and the device-side bounded-wait failure path."""
+import math
+
+import pytest
+import torch
+
+import exact_second_order_two_gb300 as fbob
+from exact_second_order_two_gb300.synthetic import Workload, make_inputs
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
+
+GUARD = 4096  # elements of guard region after every output
+
+
+def guarded(like: torch.Tensor, fill=float("nan")):
+    """A NaN-filled output tensor followed by a guard region in one buffer."""
+    buf = torch.full((like.numel() + GUARD,), fill, dtype=like.dtype, device=like.device)
+    return buf, buf[: like.numel()].view(like.shape)
+
+
+@pytest.mark.parametrize("d,dtype,N", [(64, torch.bfloat16, 200), (128, torch.bfloat16, 333),
+                                       (64, torch.float32, 77), (128, torch.bfloat16, 4096)])
+def test_outputs_fully_written_and_guards_intact(d, dtype, N):
+    w = Workload("canary", 1, 3, N, d, "bf16" if dtype == torch.bfloat16 else "fp32",
+                 True, 1.0, 1.0, 0.2)
+    ins = {k: v.cuda() for k, v in make_inputs(w, seed=11).items()}
+    q = ins["q"]
+    o_buf, o = guarded(q)
+    lse_buf, lse = guarded(torch.empty(q.shape[:3], dtype=torch.float32, device="cuda"))
+    fbob.forward(q, ins["k"], ins["v"], True, w.scale, out=(o, lse))
+    bufs = [guarded(q) for _ in range(4)]
+    fbob.bob(q, ins["k"], ins["v"], o, lse, ins["do"], ins["gq"], ins["gk"], ins["gv"],
+             True, w.scale, out=tuple(b[1] for b in bufs))
+    gbufs = [guarded(q) for _ in range(3)]
+    fbob.backward(q, ins["k"], ins["v"], o, lse, ins["do"], True, w.scale,
+                  out=tuple(b[1] for b in gbufs))
+    torch.cuda.synchronize()
+    for buf, view in [(o_buf, o), (lse_buf, lse)] + bufs + gbufs:
+        assert torch.isfinite(view.float()).all()
+        assert torch.isnan(buf[view.numel():].float()).all()
+
+
+def test_workspace_guard_and_status():
+    w = Workload("ws", 1, 2, 300, 128, "bf16", True, 1.0, 1.0, 0.2)
+    ins = {k: v.cuda() for k, v in make_inputs(w, seed=12).items()}
+    shp = fbob.shape_of(ins["q"], True, w.scale)
+    need = fbob.workspace_size(fbob.OP_BOB, shp)
+    ws_buf = torch.full((need + 8192,), 0x5A, dtype=torch.uint8, device="cuda")
+    ws = ws_buf[:need]
+    o, lse = fbob.forward(ins["q"], ins["k"], ins["v"], True, w.scale)
+    fbob.bob(ins["q"], ins["k"], ins["v"], o, lse, ins["do"], ins["gq"], ins["gk"],
+             ins["gv"], True, w.scale, workspace=ws)
+    assert fbob.status(ws) == 0
+    assert (ws_buf[need:] == 0x5A).all()
+
+
+def test_workspace_too_small_is_rejected():
+    w = Workload("ws", 1, 1, 64, 64, "bf16", True, 1.0, 1.0, 0.2)
+    ins = {k: v.cuda() for k, v in make_inputs(w, seed=1).items()}
+    o, lse = fbob.forward(ins["q"], ins["k"], ins["v"], True, w.scale)
+    shp = fbob.shape_of(ins["q"], True, w.scale)
+    small = torch.empty(fbob.workspace_size(fbob.OP_BOB, shp) - 256, dtype=torch.uint8,
+                        device="cuda")
+    with pytest.raises(fbob.FbobError) as e:
+        fbob.bob(ins["q"], ins["k"], ins["v"], o, lse, ins["do"], ins["gq"], ins["gk"],
+                 ins["gv"], True, w.scale, workspace=small)
+    assert e.value.code == 3
+
+
+def test_unsupported_head_dim_is_rejected():
+    q = torch.zeros(1, 1, 8, 256, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fbob.FbobError) as e:
+        fbob.forward(q, q, q, True, 1 / math.sqrt(256))
+    assert e.value.code == 2
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    assert fbob.selftest_wait_timeout(ws, 2000) == 5  # FBOB_ERR_TIMEOUT
+    # the context is still usable afterwards
+    w = Workload("after", 1, 1, 64, 64, "bf16", True, 1.0, 1.0, 0.2)
+    ins = {k: v.cuda() for k, v in make_inputs(w, seed=2).items()}
+    o, lse = fbob.forward(ins["q"], ins["k"], ins["v"], True, w.scale)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o.float()).all()
+
+
+def test_launch_count_is_reported():
+    w = Workload("count", 1, 1, 128, 64, "bf16", True, 1.0, 1.0, 0.2)
+    ins = {k: v.cuda() for k, v in make_inputs(w, seed=3).items()}
+    o, lse = fbob.forward(ins["q"], ins["k"], ins["v"], True, w.scale)
+    fbob.bob(ins["q"], ins["k"], ins["v"], o, lse, ins["do"], ins["gq"], ins["gk"],
+             ins["gv"], True, w.scale)
+    assert fbob.last_launch_count() >= 2
