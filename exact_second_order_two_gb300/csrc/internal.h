@@ -51,14 +51,7 @@ cudaError_t simt_bob(const Problem& p, const void* q, const void* k,
                      void* graddo, const Workspace& ws, LaunchLog& log);
 
 // ---- tensor-core (tcgen05 / TMEM / TMA) kernels, bf16, d in {64, 128} ----
-bool tc_supported(const Problem& p);
-cudaError_t tc_forward(const Problem& p, const void* q, const void* k,
-                       const void* v, void* o, float* lse, const Workspace& ws,
-                       LaunchLog& log);
-cudaError_t tc_backward(const Problem& p, const void* q, const void* k,
-                        const void* v, const void* o, const float* lse,
-                        const void* dO, void* dq, void* dk, void* dv,
-                        const Workspace& ws, LaunchLog& log);
+bool tc_supported(const Problem& p);  // BoB only
 cudaError_t tc_bob(const Problem& p, const void* q, const void* k,
                    const void* v, const void* o, const float* lse,
                    const void* dO, const void* gq, const void* gk,

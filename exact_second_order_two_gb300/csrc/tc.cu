@@ -1,12 +1,857 @@
-// Tensor-core (tcgen05 / TMEM / TMA) kernels for sm_103a.
+// Tensor-core (tcgen05 / TMEM / TMA) kernels for sm_103a: the two-pass
+// exact backward-over-backward of softmax attention.
+//
+// FlashBoB ("FlashBoB: I/O-Efficient Exact Backward-over-Backward for
+// Softmax Attention", Abstract) observes that two row-wise scalars determine
+// every BoB output through affine maps.  With c the scale,
+//   S = c Q K^T, P = exp(S - LSE), dP = dO V^T, D_i = dO_i . O_i,
+//   G = c (Q gK^T + gQ K^T)   (cotangent of dS),   H = dO gV^T,
+//   r_i = sum_j P_ij G_ij,
+//   graddO = P gV + (P*G) V - r O,      sigma_i = dO_i . graddO_i,
+//   dS  = P*(dP - D),  gdP = P*(G - r),  gS = P*(H + (G - r)*(dP - D) - sigma),
+//   gradQ = c (gS K + dS gK),  gradK = c (gS^T Q + dS^T gQ),  gradV = gdP^T dO.
+// (Derived for this library; the pages print no equations.)  The schedule:
+//
+//   pass 1 (row-stationary, 128 query rows per CTA, 64-key tiles streamed):
+//     S and G on the tensor cores into TMEM, P and P*G in registers (bf16 to
+//     shared memory), W += P gV + (P*G) V into TMEM; epilogue r, D, sigma,
+//     graddO = W - r O.
+//   pass 2 (key-stationary, 128 key rows per CTA, 64-query tiles streamed):
+//     S^T, dP^T, G^T, H^T into TMEM; dS^T, gdP^T, gS^T in registers (bf16 to
+//     shared memory); gradV += gdP^T dO and gradK += gS^T Q + dS^T gQ in
+//     TMEM; gradQ^T partial = K^T gS^T + gK^T dS^T into TMEM, reduced into an
+//     fp32 accumulator with vector-free red.global.add.
+//   convert: fp32 gradQ accumulator -> bf16.
+//
+// No N x N tensor ever leaves TMEM / shared memory / registers.  Warp roles
+// per CTA: warps 0-7 elementwise (thread = TMEM lane; warps w and w+4 split
+// the 64 tile columns), warp 8 TMA producer, warp 9 TMEM allocator and
+// single-thread MMA issuer.  Every wait is bounded (see common.cuh).
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "sm103.cuh"
 
 namespace fbob {
 
+using namespace sm103;
+
 namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// MN-major operand descriptor convention: LBO = stride between 64-element
+// groups along M/N, SBO = stride between 8-row groups along K.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
+  return sdesc_sw128(saddr, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr, uint32_t mn_group_stride) {
+  return sdesc_sw128(saddr, mn_group_stride, 1024);
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        report_status(status, FBOB_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform bounded wait: tcgen05.ld is .sync.aligned, so every lane of
+// a warp must take the same branch after a wait.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  const bool ok = wait_bar(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+// K-major tile [rows][D] stored as D/64 boxes of [rows][64] (128 B rows,
+// 128-byte swizzle).  Descriptor for the k-th 16-element slice along D.
+__device__ __forceinline__ uint64_t kslice(uint32_t base, int rows, int k) {
+  return desc_kmajor(base + (uint32_t)((k >> 2) * rows * 128 + (k & 3) * 32));
+}
+
+// 16 consecutive bf16 (one thread's half-row chunk) -> swizzled smem row.
+__device__ __forceinline__ void store_row_chunk(uint32_t tile, uint32_t row, uint32_t chunk0,
+                                                const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    st_shared_v4(tile + sw128_offset(row, chunk0 + q), w[4 * q], w[4 * q + 1], w[4 * q + 2],
+                 w[4 * q + 3]);
+}
+
+// ===========================================================================
+// Pass 1: row-stationary.
+// ===========================================================================
+template <int D>
+struct Row {
+  static constexpr int BM = 128, BN = 64;
+  static constexpr int STAGES = D == 128 ? 2 : 3;
+  static constexpr uint32_t QB = BM * D * 2;        // Q or gQ tile
+  static constexpr uint32_t KB = BN * D * 2;        // one streamed key-side tile
+  static constexpr uint32_t SB = 4 * KB;            // stage: K, gK, V, gV
+  static constexpr uint32_t PB = BM * BN * 2;       // P or P*G tile
+  static constexpr uint32_t OFF_Q = 0, OFF_GQ = QB, OFF_ST = 2 * QB;
+  static constexpr uint32_t OFF_P = OFF_ST + STAGES * SB, OFF_PG = OFF_P + PB;
+  static constexpr uint32_t OFF_MISC = OFF_PG + PB;  // barriers, TMEM slot, abort flag
+  static constexpr uint32_t MISC = 512;
+  static constexpr uint32_t SMEM = OFF_MISC + MISC;
+  static_assert(SMEM <= 232448, "pass 1 shared memory budget");
+  // TMEM columns
+  // S and G of tile buffer b at columns 128b and 128b + 64
+  __host__ __device__ static constexpr uint32_t T_S(int b) { return 128u * b; }
+  __host__ __device__ static constexpr uint32_t T_G(int b) { return 128u * b + 64u; }
+  static constexpr uint32_t T_W = 256, TMEM_COLS = 512;
+};
+
+struct RowParams {
+  const float* lse;
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dO;
+  __nv_bfloat16* graddo;
+  float* r_out;
+  float* sigma_out;
+  float* D_out;
+  float* acc_zero;  // fp32 gradQ accumulator rows to clear (may be null)
+  int* status;
+  int N, causal;
+  float scale;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bob_row_pass(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mGQ,
+                 const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mGK,
+                 const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mGV,
+                 RowParams prm) {
+  using C = Row<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {  // 128-byte swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) report_status(prm.status, FBOB_ERR_CUDA);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;                  // [STAGES]
+  uint64_t* kv_empty = bars + 1 + C::STAGES;     // [STAGES]
+  uint64_t* sg_full = bars + 1 + 2 * C::STAGES;  // [2]
+  uint64_t* sg_empty = sg_full + 2;              // [2]
+  uint64_t* p_full = sg_empty + 2;
+  uint64_t* p_empty = p_full + 1;
+  uint64_t* w_done = p_empty + 1;
+  uint64_t* drain = w_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
+  // epilogue partial sums [4][128] reuse the P tile once the last W MMA is done
+  float* part = reinterpret_cast<float*>(smem + C::OFF_P);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = prm.N;
+  const int bh = blockIdx.y;
+  // heavy (late) row blocks first under a causal mask
+  const int nblk = gridDim.x;
+  const int blk = prm.causal ? (nblk - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int i0 = blk * C::BM;
+  const int kend = prm.causal ? min(N, i0 + C::BM) : N;
+  const int T = (kend + C::BN - 1) / C::BN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(kv_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sg_full + b, 1);
+      mbar_init(sg_empty + b, kConsumers);
+    }
+    mbar_init(p_full, kConsumers);
+    mbar_init(p_empty, 1);
+    mbar_init(w_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mK);
+      mbar_arrive_expect_tx(q_full, 2 * C::QB);
+      for (int b = 0; b < D / 64; ++b) {
+        tma_load_3d(smem + C::OFF_Q + b * C::BM * 128, &mQ, q_full, 64 * b, i0, bh);
+        tma_load_3d(smem + C::OFF_GQ + b * C::BM * 128, &mGQ, q_full, 64 * b, i0, bh);
+      }
+      int issued = 0;
+      for (int t = 0; t < T; ++t, ++issued) {
+        const int s = t % C::STAGES;
+        if (t >= C::STAGES &&
+            !wait_bar(kv_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status))
+          break;
+        uint8_t* st = smem + C::OFF_ST + s * C::SB;
+        mbar_arrive_expect_tx(kv_full + s, C::SB);
+        for (int b = 0; b < D / 64; ++b) {
+          const uint32_t bo = b * C::BN * 128;
+          tma_load_3d(st + 0 * C::KB + bo, &mK, kv_full + s, 64 * b, t * C::BN, bh);
+          tma_load_3d(st + 1 * C::KB + bo, &mGK, kv_full + s, 64 * b, t * C::BN, bh);
+          tma_load_3d(st + 2 * C::KB + bo, &mV, kv_full + s, 64 * b, t * C::BN, bh);
+          tma_load_3d(st + 3 * C::KB + bo, &mGV, kv_full + s, 64 * b, t * C::BN, bh);
+        }
+      }
+      // after an abort, loads still in flight must land before the CTA exits
+      if (*abort_flag) {
+        mbar_wait_bounded(q_full, 0, prm.status, 100000000ull);
+        for (int t = max(0, issued - C::STAGES); t < issued; ++t)
+          mbar_wait_bounded(kv_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+                            100000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);  // S, G: M=128 N=64
+      constexpr uint32_t id_w = idesc_bf16(128, D, false, true);    // W: N=D, B MN-major
+      const uint32_t q_s = sb + C::OFF_Q, gq_s = sb + C::OFF_GQ;
+      const uint32_t p_s = sb + C::OFF_P, pg_s = sb + C::OFF_PG;
+      bool ok = wait_bar(q_full, 0, abort_flag, prm.status);
+      auto issue_w = [&](int t) {
+        const uint32_t st = sb + C::OFF_ST + (t % C::STAGES) * C::SB;
+        const uint32_t v_s = st + 2 * C::KB, gv_s = st + 3 * C::KB;
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 keys
+          mma_bf16(tmem + C::T_W, desc_kmajor(p_s + k * 32), desc_mnmajor(gv_s + k * 2048, C::BN * 128),
+                   id_w, (t > 0 || k > 0) ? 1u : 0u);
+          mma_bf16(tmem + C::T_W, desc_kmajor(pg_s + k * 32), desc_mnmajor(v_s + k * 2048, C::BN * 128),
+                   id_w, 1u);
+        }
+        mma_commit(p_empty);
+        mma_commit(kv_empty + (t % C::STAGES));
+      };
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t % C::STAGES, b = t & 1;
+        if (!wait_bar(kv_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (t >= 2 && !wait_bar(sg_empty + b, ((t >> 1) - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t st = sb + C::OFF_ST + s * C::SB;
+        const uint32_t k_s = st, gk_s = st + C::KB;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + C::T_S(b), kslice(q_s, C::BM, k), kslice(k_s, C::BN, k), id_s, k > 0);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + C::T_G(b), kslice(q_s, C::BM, k), kslice(gk_s, C::BN, k), id_s, k > 0);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + C::T_G(b), kslice(gq_s, C::BM, k), kslice(k_s, C::BN, k), id_s, 1u);
+        mma_commit(sg_full + b);
+        if (t >= 1) {
+          if (!wait_bar(p_full, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+          tc_fence_after();
+          issue_w(t - 1);
+        }
+      }
+      if (ok && wait_bar(p_full, (T - 1) & 1, abort_flag, prm.status)) {
+        tc_fence_after();
+        issue_w(T - 1);
+        mma_commit(w_done);
+      }
+      // every MMA this thread issued has completed before TMEM is released
+      mma_commit(drain);
+      mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
+    }
+  } else {
+    // ---------------- elementwise warps: thread = query row --------------
+    const int row = 32 * (warp & 3) + lane;
+    const int half = warp >> 2;  // columns [32*half, 32*half + 32) of a tile
+    const int i = i0 + row;
+    const bool row_ok = i < N;
+    const size_t srow = (size_t)bh * N + (row_ok ? i : 0);
+    const float lse2 = row_ok ? prm.lse[srow] * kLog2e : 0.f;
+    const float sc2 = prm.scale * kLog2e;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    float r_acc = 0.f;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int b = t & 1;
+      if (!warp_wait(sg_full + b, (t >> 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[32], gr[32];
+      tmem_ld32(tmem + lane_off + C::T_S(b) + 32 * half, sr);
+      tmem_ld32(tmem + lane_off + C::T_G(b) + 32 * half, gr);
+      tc_fence_before();
+      mbar_arrive(sg_empty + b);
+      const int j0 = t * C::BN + 32 * half;
+      const bool need_mask = !row_ok || (j0 + 32 > N) || (prm.causal && j0 + 31 > i0);
+      uint32_t pw[16], pgw[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float p0 = exp2f(__uint_as_float(sr[c]) * sc2 - lse2);
+        float p1 = exp2f(__uint_as_float(sr[c + 1]) * sc2 - lse2);
+        if (need_mask) {
+          const int j = j0 + c;
+          if (!(row_ok && j < N && (!prm.causal || j <= i))) p0 = 0.f;
+          if (!(row_ok && j + 1 < N && (!prm.causal || j + 1 <= i))) p1 = 0.f;
+        }
+        const float g0 = p0 * (__uint_as_float(gr[c]) * prm.scale);
+        const float g1 = p1 * (__uint_as_float(gr[c + 1]) * prm.scale);
+        r_acc += g0 + g1;
+        pw[c >> 1] = pack_bf16(p0, p1);
+        pgw[c >> 1] = pack_bf16(g0, g1);
+      }
+      if (t >= 1 && !warp_wait(p_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+      store_row_chunk(sb + C::OFF_P, row, 4 * half, pw);
+      store_row_chunk(sb + C::OFF_PG, row, 4 * half, pgw);
+      fence_async_smem();
+      mbar_arrive(p_full);
+    }
+    // ---- epilogue: r, D, sigma, graddO = W - r O ----
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) ok = warp_wait(w_done, 0, abort_flag, prm.status);
+    tc_fence_after();
+    consumer_sync();  // P is dead for every thread before it is reused
+    part[half * 128 + row] = r_acc;
+    consumer_sync();
+    const float r = part[row] + part[128 + row];
+    float dd = 0.f, sg = 0.f;
+    if (ok) {
+      constexpr int HALF = D / 2;
+      const size_t obase = srow * D + HALF * half;
+#pragma unroll
+      for (int cc = 0; cc < HALF; cc += 32) {
+        uint32_t wr[32];
+        tmem_ld32(tmem + lane_off + C::T_W + HALF * half + cc, wr);
+        if (row_ok) {
+          const uint4* op = reinterpret_cast<const uint4*>(prm.o + obase + cc);
+          const uint4* dp = reinterpret_cast<const uint4*>(prm.dO + obase + cc);
+          uint4* gp = reinterpret_cast<uint4*>(prm.graddo + obase + cc);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 ov = op[v], dv = dp[v];
+            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+            const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+            uint32_t outw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 of = __bfloat1622float2(o2[e]);
+              const float2 df = __bfloat1622float2(d2[e]);
+              const float w0 = __uint_as_float(wr[8 * v + 2 * e]) - r * of.x;
+              const float w1 = __uint_as_float(wr[8 * v + 2 * e + 1]) - r * of.y;
+              dd = fmaf(df.x, of.x, fmaf(df.y, of.y, dd));
+              sg = fmaf(df.x, w0, fmaf(df.y, w1, sg));
+              outw[e] = pack_bf16(w0, w1);
+            }
+            gp[v] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    consumer_sync();  // everyone has read `part` for r
+    part[half * 128 + row] = dd;
+    part[256 + half * 128 + row] = sg;
+    consumer_sync();
+    if (ok && half == 0 && row_ok) {
+      prm.r_out[srow] = r;
+      prm.D_out[srow] = part[row] + part[128 + row];
+      prm.sigma_out[srow] = part[256 + row] + part[384 + row];
+    }
+    // clear this row's fp32 gradQ accumulator for the key-stationary pass
+    if (prm.acc_zero && row_ok) {
+      float4* a = reinterpret_cast<float4*>(prm.acc_zero + srow * D + (D / 2) * half);
+#pragma unroll
+      for (int v = 0; v < D / 8; ++v) a[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ===========================================================================
+// Pass 2: key-stationary.
+// ===========================================================================
+template <int D>
+struct Col {
+  static constexpr int BM = 128, BN = 64;
+  static constexpr int STAGES = D == 128 ? 1 : 2;
+  static constexpr uint32_t KB = BM * D * 2;     // stationary K, gK, V, gV tile
+  static constexpr uint32_t QB = BN * D * 2;     // streamed Q, gQ, dO tile
+  static constexpr uint32_t SB = 3 * QB;
+  static constexpr uint32_t XB = BM * BN * 2;    // dS^T / gdP^T / gS^T tile
+  static constexpr uint32_t OFF_K = 0, OFF_GK = KB, OFF_V = 2 * KB, OFF_GV = 3 * KB;
+  static constexpr uint32_t OFF_ST = 4 * KB;
+  static constexpr uint32_t OFF_DS = OFF_ST + STAGES * SB, OFF_GDP = OFF_DS + XB,
+                            OFF_GS = OFF_GDP + XB;
+  static constexpr uint32_t OFF_SC = OFF_GS + XB;          // [STAGES][4][BN] fp32
+  static constexpr uint32_t OFF_MISC = OFF_SC + STAGES * 4 * BN * 4;
+  static constexpr uint32_t MISC = 512;
+  static constexpr uint32_t SMEM = OFF_MISC + MISC;
+  static_assert(SMEM <= 232448, "pass 2 shared memory budget");
+  // TMEM columns
+  static constexpr uint32_t T_S = 0, T_DP = 64, T_G = 128, T_H = 192, T_GK = 256, T_GV = 256 + D;
+  static constexpr bool GQ_IN_H = (256 + 2 * D + 64 > 512);
+  static constexpr uint32_t T_GQ = GQ_IN_H ? T_H : 256 + 2 * D;
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+
+struct ColParams {
+  const float* lse;
+  const float* Dv;
+  const float* r;
+  const float* sigma;
+  __nv_bfloat16* gradk;
+  __nv_bfloat16* gradv;
+  float* acc;  // fp32 [B,H,N,D] gradQ accumulator
+  int* status;
+  int N, causal;
+  float scale;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bob_col_pass(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mGK,
+                 const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mGV,
+                 const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mGQ,
+                 const __grid_constant__ CUtensorMap mDO, ColParams prm) {
+  using C = Col<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {  // 128-byte swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) report_status(prm.status, FBOB_ERR_CUDA);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* st_full = bars + 1;                 // [STAGES]
+  uint64_t* st_empty = bars + 1 + C::STAGES;    // [STAGES]  (MMA commit + consumers)
+  uint64_t* sc_full = bars + 1 + 2 * C::STAGES;
+  uint64_t* sc_empty = sc_full + 1;
+  uint64_t* ds_full = sc_empty + 1;
+  uint64_t* gq_full = ds_full + 1;
+  uint64_t* gq_empty = gq_full + 1;
+  uint64_t* acc_done = gq_empty + 1;
+  uint64_t* drain = acc_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
+  float* scal = reinterpret_cast<float*>(smem + C::OFF_SC);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = prm.N;
+  const int bh = blockIdx.y;
+  const int j0 = (int)blockIdx.x * C::BM;  // low key blocks (most query tiles) first
+  const int qstart = prm.causal ? (j0 / C::BN) * C::BN : 0;
+  const int T = (N - qstart + C::BN - 1) / C::BN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(st_full + s, 1);
+      mbar_init(st_empty + s, 1 + kConsumers);
+    }
+    mbar_init(sc_full, 1);
+    mbar_init(sc_empty, kConsumers);
+    mbar_init(ds_full, kConsumers);
+    mbar_init(gq_full, 1);
+    mbar_init(gq_empty, kConsumers);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 4 * C::KB);
+      for (int b = 0; b < D / 64; ++b) {
+        const uint32_t bo = b * C::BM * 128;
+        tma_load_3d(smem + C::OFF_K + bo, &mK, kv_full, 64 * b, j0, bh);
+        tma_load_3d(smem + C::OFF_GK + bo, &mGK, kv_full, 64 * b, j0, bh);
+        tma_load_3d(smem + C::OFF_V + bo, &mV, kv_full, 64 * b, j0, bh);
+        tma_load_3d(smem + C::OFF_GV + bo, &mGV, kv_full, 64 * b, j0, bh);
+      }
+    }
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % C::STAGES;
+      const int q0 = qstart + t * C::BN;
+      if (t >= C::STAGES) {
+        bool w = true;
+        if (lane == 0) w = wait_bar(st_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      // row scalars of this query tile (lse pre-scaled by log2 e)
+      float* sc = scal + s * 4 * C::BN;
+      for (int e = lane; e < C::BN; e += 32) {
+        const int q = q0 + e;
+        const bool in = q < N;
+        const size_t idx = (size_t)bh * N + (in ? q : 0);
+        sc[e] = in ? prm.lse[idx] * kLog2e : 0.f;
+        sc[C::BN + e] = in ? prm.Dv[idx] : 0.f;
+        sc[2 * C::BN + e] = in ? prm.r[idx] : 0.f;
+        sc[3 * C::BN + e] = in ? prm.sigma[idx] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        uint8_t* st = smem + C::OFF_ST + s * C::SB;
+        mbar_arrive_expect_tx(st_full + s, C::SB);
+        for (int b = 0; b < D / 64; ++b) {
+          const uint32_t bo = b * C::BN * 128;
+          tma_load_3d(st + 0 * C::QB + bo, &mQ, st_full + s, 64 * b, q0, bh);
+          tma_load_3d(st + 1 * C::QB + bo, &mGQ, st_full + s, 64 * b, q0, bh);
+          tma_load_3d(st + 2 * C::QB + bo, &mDO, st_full + s, 64 * b, q0, bh);
+        }
+      }
+    }
+    if (lane == 0) {
+      wait_bar(kv_full, 0, abort_flag, prm.status);
+      if (*abort_flag)
+        for (int t = max(0, T - C::STAGES); t < T; ++t)
+          mbar_wait_bounded(st_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+                            100000000ull);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t id_sc = idesc_bf16(128, 64, false, false);  // scores: M=128 N=64
+      constexpr uint32_t id_out = idesc_bf16(128, D, false, true);   // gradK/V: N=D, B MN
+      constexpr uint32_t id_gq = idesc_bf16(D, 64, true, true);      // gradQ^T: M=D, A,B MN
+      const uint32_t k_s = sb + C::OFF_K, gk_s = sb + C::OFF_GK, v_s = sb + C::OFF_V,
+                     gv_s = sb + C::OFF_GV;
+      const uint32_t ds_s = sb + C::OFF_DS, gdp_s = sb + C::OFF_GDP, gs_s = sb + C::OFF_GS;
+      bool ok = wait_bar(kv_full, 0, abort_flag, prm.status);
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t % C::STAGES;
+        const uint32_t st = sb + C::OFF_ST + s * C::SB;
+        const uint32_t q_s = st, gq_s = st + C::QB, do_s = st + 2 * C::QB;
+        if (!wait_bar(st_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (t >= 1 && !wait_bar(sc_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + C::T_S, kslice(k_s, C::BM, k), kslice(q_s, C::BN, k), id_sc, k > 0);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + C::T_G, kslice(gk_s, C::BM, k), kslice(q_s, C::BN, k), id_sc, k > 0);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + C::T_G, kslice(k_s, C::BM, k), kslice(gq_s, C::BN, k), id_sc, 1u);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + C::T_DP, kslice(v_s, C::BM, k), kslice(do_s, C::BN, k), id_sc, k > 0);
+        if (C::GQ_IN_H && t >= 1) {
+          if (!wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + C::T_H, kslice(gv_s, C::BM, k), kslice(do_s, C::BN, k), id_sc, k > 0);
+        mma_commit(sc_full);
+        // ---- outputs: wait for dS^T, gdP^T, gS^T in shared memory ----
+        if (!wait_bar(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 queries
+          const uint32_t ko = k * 32, kr = k * 2048;
+          mma_bf16(tmem + C::T_GV, desc_kmajor(gdp_s + ko), desc_mnmajor(do_s + kr, C::BN * 128),
+                   id_out, (t > 0 || k > 0) ? 1u : 0u);
+          mma_bf16(tmem + C::T_GK, desc_kmajor(gs_s + ko), desc_mnmajor(q_s + kr, C::BN * 128),
+                   id_out, (t > 0 || k > 0) ? 1u : 0u);
+          mma_bf16(tmem + C::T_GK, desc_kmajor(ds_s + ko), desc_mnmajor(gq_s + kr, C::BN * 128),
+                   id_out, 1u);
+        }
+        mma_commit(st_empty + s);
+        if (!C::GQ_IN_H && t >= 1) {
+          if (!wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int k = 0; k < C::BM / 16; ++k) {  // contraction over the 128 keys
+          const uint32_t kr = k * 2048;
+          mma_bf16(tmem + C::T_GQ, desc_mnmajor(k_s + kr, C::BM * 128),
+                   desc_mnmajor(gs_s + kr, 1024), id_gq, k > 0);
+          mma_bf16(tmem + C::T_GQ, desc_mnmajor(gk_s + kr, C::BM * 128),
+                   desc_mnmajor(ds_s + kr, 1024), id_gq, 1u);
+        }
+        mma_commit(gq_full);
+      }
+      if (ok) mma_commit(acc_done);
+      mma_commit(drain);
+      mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
+    }
+  } else {
+    // ---------------- elementwise warps: thread = key row -----------------
+    const int row = 32 * (warp & 3) + lane;
+    const int half = warp >> 2;
+    const int j = j0 + row;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const float sc2 = prm.scale * kLog2e;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % C::STAGES;
+      const int q0 = qstart + t * C::BN;
+      if (!warp_wait(sc_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[32], dpr[32], gr[32], hr[32];
+      tmem_ld32(tmem + lane_off + C::T_S + 32 * half, sr);
+      tmem_ld32(tmem + lane_off + C::T_DP + 32 * half, dpr);
+      tmem_ld32(tmem + lane_off + C::T_G + 32 * half, gr);
+      tmem_ld32(tmem + lane_off + C::T_H + 32 * half, hr);
+      tc_fence_before();
+      mbar_arrive(sc_empty);
+      const float* sc = scal + s * 4 * C::BN + 32 * half;
+      const int qa = q0 + 32 * half;
+      const bool need_mask = (qa + 32 > N) || (j0 + C::BM > N) || (prm.causal && qa < j0 + C::BM);
+      uint32_t dsw[16], gdw[16], gsw[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float o_ds[2], o_gd[2], o_gs[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int cc = c + e;
+          float p = exp2f(__uint_as_float(sr[cc]) * sc2 - sc[cc]);
+          if (need_mask) {
+            const int q = qa + cc;
+            if (!(q < N && j < N && (!prm.causal || q >= j))) p = 0.f;
+          }
+          const float dpm = __uint_as_float(dpr[cc]) - sc[C::BN + cc];
+          const float gm = __uint_as_float(gr[cc]) * prm.scale - sc[2 * C::BN + cc];
+          o_ds[e] = p * dpm;
+          o_gd[e] = p * gm;
+          o_gs[e] = p * (__uint_as_float(hr[cc]) + gm * dpm - sc[3 * C::BN + cc]);
+        }
+        dsw[c >> 1] = pack_bf16(o_ds[0], o_ds[1]);
+        gdw[c >> 1] = pack_bf16(o_gd[0], o_gd[1]);
+        gsw[c >> 1] = pack_bf16(o_gs[0], o_gs[1]);
+      }
+      // ds buffers of tile t-1 were released by gq_full(t-1), awaited below
+      store_row_chunk(sb + C::OFF_DS, row, 4 * half, dsw);
+      store_row_chunk(sb + C::OFF_GDP, row, 4 * half, gdw);
+      store_row_chunk(sb + C::OFF_GS, row, 4 * half, gsw);
+      fence_async_smem();
+      mbar_arrive(ds_full);
+      mbar_arrive(st_empty + s);  // this thread is done with the stage's scalars
+      // ---- gradQ^T partial: TMEM lane = feature index, column = query ----
+      if (!warp_wait(gq_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+      tc_fence_after();
+      if (D == 128) {
+        uint32_t gq[32];
+        tmem_ld32(tmem + lane_off + C::T_GQ + 32 * half, gq);
+        const int dcol = row;
+        float* base = prm.acc + ((size_t)bh * N + qa) * D + dcol;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
+      } else {
+        // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
+        // lanes 32w' + x; the upper 16 lanes of each warp hold nothing.
+        uint32_t gq[32];
+        tmem_ld32(tmem + lane_off + C::T_GQ + 32 * half, gq);
+        if (lane < 16) {
+          const int dcol = 16 * (warp & 3) + lane;
+          float* base = prm.acc + ((size_t)bh * N + qa) * D + dcol;
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(gq_empty);
+    }
+    // ---- epilogue: gradK (scaled), gradV ----
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) ok = warp_wait(acc_done, 0, abort_flag, prm.status);
+    tc_fence_after();
+    if (ok) {  // warp-uniform: every lane loads TMEM, rows past N do not store
+      constexpr int HALF = D / 2;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* out = which == 0 ? prm.gradk : prm.gradv;
+        const float mul = which == 0 ? prm.scale : 1.f;
+        const uint32_t tcol = (which == 0 ? C::T_GK : C::T_GV) + HALF * half;
+        uint4* op = reinterpret_cast<uint4*>(out + ((size_t)bh * N + j) * D + HALF * half);
+#pragma unroll
+        for (int cc = 0; cc < HALF; cc += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + tcol + cc, v);
+          if (j < N) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w4[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]) * mul,
+                                  __uint_as_float(v[8 * q + 2 * e + 1]) * mul);
+              op[cc / 8 + q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// fp32 accumulator -> bf16, 8 elements per thread.
+__global__ void __launch_bounds__(256) gradq_convert(const float4* __restrict__ acc,
+                                                     uint4* __restrict__ out, size_t n8) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    out[i] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
+                        pack_bf16(b.z, b.w));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [B*H, N, D] bf16 tensor, box = 64 features x box_rows rows, 128-byte swizzle;
+// rows past N read as zero.
+bool make_map(CUtensorMap* m, const void* ptr, const Problem& p, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.N, (cuuint64_t)p.BH()};
+  cuuint64_t strides[2] = {(cuuint64_t)p.d * 2, (cuuint64_t)p.N * p.d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v, const void* o,
+                  const float* lse, const void* dO, const void* gq, const void* gk,
+                  const void* gv, void* gradq, void* gradk, void* gradv, void* graddo,
+                  const Workspace& ws, LaunchLog& log) {
+  using R = Row<D>;
+  using Cc = Col<D>;
+  CUtensorMap mQr, mGQr, mKr, mGKr, mVr, mGVr;
+  if (!make_map(&mQr, q, p, R::BM) || !make_map(&mGQr, gq, p, R::BM) ||
+      !make_map(&mKr, k, p, R::BN) || !make_map(&mGKr, gk, p, R::BN) ||
+      !make_map(&mVr, v, p, R::BN) || !make_map(&mGVr, gv, p, R::BN))
+    return cudaErrorInvalidValue;
+  CUtensorMap mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc;
+  if (!make_map(&mKc, k, p, Cc::BM) || !make_map(&mGKc, gk, p, Cc::BM) ||
+      !make_map(&mVc, v, p, Cc::BM) || !make_map(&mGVc, gv, p, Cc::BM) ||
+      !make_map(&mQc, q, p, Cc::BN) || !make_map(&mGQc, gq, p, Cc::BN) ||
+      !make_map(&mDOc, dO, p, Cc::BN))
+    return cudaErrorInvalidValue;
+
+  cudaError_t e = cudaFuncSetAttribute(bob_row_pass<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)R::SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bob_col_pass<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)Cc::SMEM);
+  if (e != cudaSuccess) return e;
+
+  RowParams rp;
+  rp.lse = lse;
+  rp.o = static_cast<const __nv_bfloat16*>(o);
+  rp.dO = static_cast<const __nv_bfloat16*>(dO);
+  rp.graddo = static_cast<__nv_bfloat16*>(graddo);
+  rp.r_out = ws.r;
+  rp.sigma_out = ws.sigma;
+  rp.D_out = ws.D;
+  rp.acc_zero = ws.acc;
+  rp.status = ws.status;
+  rp.N = p.N;
+  rp.causal = p.causal;
+  rp.scale = p.scale;
+  dim3 g1((p.N + R::BM - 1) / R::BM, p.BH());
+  bob_row_pass<D><<<g1, kThreads, R::SMEM, log.stream>>>(mQr, mGQr, mKr, mGKr, mVr, mGVr, rp);
+  e = cudaGetLastError();
+  log.mark();
+  if (e != cudaSuccess) return e;
+
+  ColParams cp;
+  cp.lse = lse;
+  cp.Dv = ws.D;
+  cp.r = ws.r;
+  cp.sigma = ws.sigma;
+  cp.gradk = static_cast<__nv_bfloat16*>(gradk);
+  cp.gradv = static_cast<__nv_bfloat16*>(gradv);
+  cp.acc = ws.acc;
+  cp.status = ws.status;
+  cp.N = p.N;
+  cp.causal = p.causal;
+  cp.scale = p.scale;
+  dim3 g2((p.N + Cc::BM - 1) / Cc::BM, p.BH());
+  bob_col_pass<D><<<g2, kThreads, Cc::SMEM, log.stream>>>(mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc, cp);
+  e = cudaGetLastError();
+  log.mark();
+  if (e != cudaSuccess) return e;
+
+  const size_t n8 = p.elems() / 8;
+  const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 152 * 16);
+  gradq_convert<<<blocks, 256, 0, log.stream>>>(reinterpret_cast<const float4*>(ws.acc),
+                                                static_cast<uint4*>(gradq), n8);
+  e = cudaGetLastError();
+  log.mark();
+  return e;
+}
 
 // One thread waits on an mbarrier whose phase nothing completes; the bounded
 // wait gives up after limit_ns and records FBOB_ERR_TIMEOUT.
@@ -14,7 +859,7 @@ __global__ void wait_timeout_selftest_kernel(int* status, unsigned long long lim
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_mbar_init();
   }
   __syncthreads();
   if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, status, limit_ns);
@@ -23,30 +868,20 @@ __global__ void wait_timeout_selftest_kernel(int* status, unsigned long long lim
 
 }  // namespace
 
-cudaError_t launch_wait_timeout_selftest(int* status, long long limit_ns,
-                                         cudaStream_t stream) {
+cudaError_t launch_wait_timeout_selftest(int* status, long long limit_ns, cudaStream_t stream) {
   wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, (unsigned long long)limit_ns);
   return cudaGetLastError();
 }
 
-bool tc_supported(const Problem&) { return false; }
+bool tc_supported(const Problem& p) { return p.bf16 && (p.d == 64 || p.d == 128); }
 
-cudaError_t tc_forward(const Problem&, const void*, const void*, const void*,
-                       void*, float*, const Workspace&, LaunchLog&) {
-  return cudaErrorNotSupported;
-}
-
-cudaError_t tc_backward(const Problem&, const void*, const void*, const void*,
-                        const void*, const float*, const void*, void*, void*,
-                        void*, const Workspace&, LaunchLog&) {
-  return cudaErrorNotSupported;
-}
-
-cudaError_t tc_bob(const Problem&, const void*, const void*, const void*,
-                   const void*, const float*, const void*, const void*,
-                   const void*, const void*, void*, void*, void*, void*,
-                   const Workspace&, LaunchLog&) {
-  return cudaErrorNotSupported;
+cudaError_t tc_bob(const Problem& p, const void* q, const void* k, const void* v, const void* o,
+                   const float* lse, const void* dO, const void* gq, const void* gk,
+                   const void* gv, void* gradq, void* gradk, void* gradv, void* graddo,
+                   const Workspace& ws, LaunchLog& log) {
+  if (p.d == 128)
+    return bob_d<128>(p, q, k, v, o, lse, dO, gq, gk, gv, gradq, gradk, gradv, graddo, ws, log);
+  return bob_d<64>(p, q, k, v, o, lse, dO, gq, gk, gv, gradq, gradk, gradv, graddo, ws, log);
 }
 
 }  // namespace fbob

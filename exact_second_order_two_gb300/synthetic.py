@@ -7,8 +7,8 @@ the same inputs without sharing any computation.
 The five workloads are the attention shapes FlashBoB is exercised on: a small
 fp32 case, and bf16 causal cases from N=4096 up to N=262144 (the longest
 sequence the FlashBoB abstract reports on one GPU).  The paper states no
-batch, head count, head dimension or value distribution; the choices here are
-stated in DESIGN.md.
+batch, head count, head dimension or value distribution; those below are this
+library's choice.
 """
 from __future__ import annotations
 
@@ -59,6 +59,11 @@ WORKLOADS = {
         Workload("bf16_causal_peaked_h8_n65536_d128", 1, 8, 65536, 128, "bf16",
                  True, 1.5, 0.1, 0.1),
         Workload("bf16_causal_h4_n262144_d64", 1, 4, 262144, 64, "bf16", True,
+                 1.0, 1.0, 0.1),
+        # profiling-sized cases (inputs still larger than L2 in total)
+        Workload("bf16_causal_h8_n8192_d128", 1, 8, 8192, 128, "bf16", True,
+                 1.0, 1.0, 0.1),
+        Workload("bf16_causal_h16_n8192_d64", 1, 16, 8192, 64, "bf16", True,
                  1.0, 1.0, 0.1),
     )
 }

@@ -22,7 +22,7 @@ all.  It writes out the plain definition instead:
                  differentiation of the first-backward lines above, one
                  adjoint line per forward line, in reverse order.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * O and LSE are functions of Q, K, V (total derivative), not free inputs.
   * LSE is the natural log of the row sum of exp of the *scaled* scores.
   * causal masking is square and top-left aligned: key j is visible to query
