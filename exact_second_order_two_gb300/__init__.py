@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     alloc_workspace,
     backward,
     bob,
+    bob_noalloc,
     force_path,
     forward,
     last_launch_count,

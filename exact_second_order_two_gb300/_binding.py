@@ -61,6 +61,7 @@ _SIGNATURES = {
     "fbob_set_profile_events": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int]),
     "fbob_last_launch_count": (ctypes.c_int, []),
     "fbob_selftest_wait_timeout": (ctypes.c_int, [_P, _SZ, ctypes.c_int, _P]),
+    "fbob_bob_noalloc": (ctypes.c_int, [_SHP] + [_P] * 13 + [_P]),
 }
 
 
@@ -207,6 +208,23 @@ def bob(q, k, v, o, lse, do, gq, gk, gv, causal: bool = False,
                           *(_ptr(t) for t in outs), _ptr(ws), ws.numel(),
                           _stream(q.device)),
            "fbob_bob")
+    return tuple(outs)
+
+
+def bob_noalloc(q, k, v, o, lse, do, gq, gk, gv, causal: bool = False,
+                scale: float | None = None, out=None):
+    """BoB through fbob_bob_noalloc: same results as ``bob``, for callers that
+    cannot allocate device memory; the scratch comes from the library's
+    fixed device array (outputs are allocated here only when ``out`` is
+    None)."""
+    _check_tensors(q, {"k": k, "v": v, "o": o, "do": do, "gq": gq, "gk": gk,
+                       "gv": gv, "lse": lse}, ("lse",))
+    shp = shape_of(q, causal, scale)
+    outs = out if out is not None else tuple(torch.empty_like(q) for _ in range(4))
+    _check(lib().fbob_bob_noalloc(ctypes.byref(shp), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                  _ptr(lse), _ptr(do), _ptr(gq), _ptr(gk), _ptr(gv),
+                                  *(_ptr(t) for t in outs), _stream(q.device)),
+           "fbob_bob_noalloc")
     return tuple(outs)
 
 

@@ -118,6 +118,40 @@ int fbob_bob(const fbob_shape_t* shape, const void* q, const void* k,
              void* gradk, void* gradv, void* graddo, void* ws,
              size_t ws_bytes, void* stream);
 
+/* Size of the fixed device scratch array behind fbob_bob_noalloc: 32 MiB. */
+#define FBOB_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* fbob_bob for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this call.  It exists for callers that are
+ * handed only their input and output buffers: plugin or custom-operator
+ * hosts that give a kernel no allocator and no workspace, and code that must
+ * not call cudaMalloc / cudaFree, which can stall the whole device or fail
+ * when a caching allocator already holds the free memory.  Arguments and
+ * results are those of fbob_bob without `ws` / `ws_bytes`; this call itself
+ * allocates nothing.
+ *
+ * Scratch comes from one array of FBOB_NOALLOC_SCRATCH_BYTES in the
+ * library's device memory, which every GPU that loads the library keeps
+ * reserved until the process exits.  The first call on a device (with that
+ * device current) looks up the array's device address; make that first call
+ * before any stream capture.  Problems whose fbob_workspace_size(
+ * FBOB_OP_BOB, shape) exceeds FBOB_NOALLOC_SCRATCH_BYTES are rejected with
+ * FBOB_ERR_WORKSPACE (the tensor-core path needs about B*H*N*(d+3)*4 bytes,
+ * i.e. at most about 125,000 rows B*H*N at d = 64 or 63,000 at d = 128; the
+ * CUDA-core path needs about B*H*N*12 bytes).  All calls share the one
+ * array, so calls that can overlap on the GPU (different streams, or host
+ * threads) race on it: serialise them.  Each call clears what must start at
+ * zero, so contents left by an earlier call do not affect the result.  The
+ * status word that device-side bounded waits write lives in that array, out
+ * of the caller's reach: check the return code and the stream's error state
+ * instead of fbob_status(). */
+int fbob_bob_noalloc(const fbob_shape_t* shape, const void* q, const void* k,
+                     const void* v, const void* o, const float* lse,
+                     const void* dO, const void* gq, const void* gk,
+                     const void* gv, void* gradq, void* gradk, void* gradv,
+                     void* graddo, void* stream);
+
 /* Synchronises `stream`, then returns the first error recorded in the
  * workspace's status word by the last call that used `ws` (FBOB_OK if none),
  * or FBOB_ERR_CUDA if the stream itself reports an error. */
