@@ -110,13 +110,18 @@ __device__ __forceinline__ void store_row_chunk(uint32_t tile, uint32_t row, uin
 template <int D>
 struct Row {
   static constexpr int BM = 128, BN = 64;
+  // Two decoupled rings: [K|gK] (read by the S/G MMAs, freed early) and
+  // [V|gV] (read by the W MMAs of the same tile, freed one tile later).
   static constexpr int STAGES = D == 128 ? 2 : 3;
   static constexpr uint32_t QB = BM * D * 2;        // Q or gQ tile
   static constexpr uint32_t KB = BN * D * 2;        // one streamed key-side tile
-  static constexpr uint32_t SB = 4 * KB;            // stage: K, gK, V, gV
+  // [K|gK] stage: interleaved per 64-feature box (128 rows per box, so one
+  // N=128 MMA sees K and gK stacked); [V|gV] stage: V then gV
+  static constexpr uint32_t SB = 2 * KB;
   static constexpr uint32_t PB = BM * BN * 2;       // P or P*G tile
-  static constexpr uint32_t OFF_Q = 0, OFF_GQ = QB, OFF_ST = 2 * QB;
-  static constexpr uint32_t OFF_P = OFF_ST + STAGES * SB, OFF_PG = OFF_P + PB;
+  static constexpr uint32_t OFF_Q = 0, OFF_GQ = QB, OFF_KG = 2 * QB;
+  static constexpr uint32_t OFF_V = OFF_KG + STAGES * SB;
+  static constexpr uint32_t OFF_P = OFF_V + STAGES * SB, OFF_PG = OFF_P + PB;
   static constexpr uint32_t OFF_MISC = OFF_PG + PB;  // barriers, TMEM slot, abort flag
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
@@ -157,9 +162,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;                  // [STAGES]
-  uint64_t* kv_empty = bars + 1 + C::STAGES;     // [STAGES]
-  uint64_t* sg_full = bars + 1 + 2 * C::STAGES;  // [2]
+  uint64_t* kg_full = bars + 1;                  // [STAGES]
+  uint64_t* kg_empty = kg_full + C::STAGES;      // [STAGES]
+  uint64_t* v_full = kg_empty + C::STAGES;       // [STAGES]
+  uint64_t* v_empty = v_full + C::STAGES;        // [STAGES]
+  uint64_t* sg_full = v_empty + C::STAGES;       // [2]
   uint64_t* sg_empty = sg_full + 2;              // [2]
   uint64_t* p_full = sg_empty + 2;
   uint64_t* p_empty = p_full + 1;
@@ -183,8 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(kv_full + s, 1);
-      mbar_init(kv_empty + s, 1);
+      mbar_init(kg_full + s, 1);
+      mbar_init(kg_empty + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sg_full + b, 1);
@@ -215,40 +224,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + C::OFF_Q + b * C::BM * 128, &mQ, q_full, 64 * b, i0, bh);
         tma_load_3d(smem + C::OFF_GQ + b * C::BM * 128, &mGQ, q_full, 64 * b, i0, bh);
       }
-      int issued = 0;
-      for (int t = 0; t < T; ++t, ++issued) {
+      // [K|gK] runs one tile ahead of [V|gV]: the S/G MMAs of tile t+1 need
+      // only K/gK, which are released as soon as the S/G MMAs of tile t-1 end
+      int kg_issued = 0, v_issued = 0;
+      auto load_kg = [&](int t) -> bool {
         const int s = t % C::STAGES;
         if (t >= C::STAGES &&
-            !wait_bar(kv_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status))
-          break;
-        uint8_t* st = smem + C::OFF_ST + s * C::SB;
-        mbar_arrive_expect_tx(kv_full + s, C::SB);
+            !wait_bar(kg_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status))
+          return false;
+        uint8_t* st = smem + C::OFF_KG + s * C::SB;
+        mbar_arrive_expect_tx(kg_full + s, C::SB);
         for (int b = 0; b < D / 64; ++b) {
           const uint32_t bo = b * C::BN * 128;
-          tma_load_3d(st + 0 * C::KB + bo, &mK, kv_full + s, 64 * b, t * C::BN, bh);
-          tma_load_3d(st + 1 * C::KB + bo, &mGK, kv_full + s, 64 * b, t * C::BN, bh);
-          tma_load_3d(st + 2 * C::KB + bo, &mV, kv_full + s, 64 * b, t * C::BN, bh);
-          tma_load_3d(st + 3 * C::KB + bo, &mGV, kv_full + s, 64 * b, t * C::BN, bh);
+          tma_load_3d(st + 2 * bo, &mK, kg_full + s, 64 * b, t * C::BN, bh);
+          tma_load_3d(st + 2 * bo + C::BN * 128, &mGK, kg_full + s, 64 * b, t * C::BN, bh);
         }
+        ++kg_issued;
+        return true;
+      };
+      auto load_v = [&](int t) -> bool {
+        const int s = t % C::STAGES;
+        if (t >= C::STAGES &&
+            !wait_bar(v_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status))
+          return false;
+        uint8_t* st = smem + C::OFF_V + s * C::SB;
+        mbar_arrive_expect_tx(v_full + s, C::SB);
+        for (int b = 0; b < D / 64; ++b) {
+          const uint32_t bo = b * C::BN * 128;
+          tma_load_3d(st + bo, &mV, v_full + s, 64 * b, t * C::BN, bh);
+          tma_load_3d(st + C::KB + bo, &mGV, v_full + s, 64 * b, t * C::BN, bh);
+        }
+        ++v_issued;
+        return true;
+      };
+      bool pok = load_kg(0);
+      for (int t = 0; pok && t < T; ++t) {
+        if (t + 1 < T && !load_kg(t + 1)) break;
+        if (!load_v(t)) break;
       }
       // after an abort, loads still in flight must land before the CTA exits
       if (*abort_flag) {
         mbar_wait_bounded(q_full, 0, prm.status, 100000000ull);
-        for (int t = max(0, issued - C::STAGES); t < issued; ++t)
-          mbar_wait_bounded(kv_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+        for (int t = max(0, kg_issued - C::STAGES); t < kg_issued; ++t)
+          mbar_wait_bounded(kg_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+                            100000000ull);
+        for (int t = max(0, v_issued - C::STAGES); t < v_issued; ++t)
+          mbar_wait_bounded(v_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
                             100000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);  // S, G: M=128 N=64
+      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);  // gQ K^T: M=128 N=64
+      constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // Q [K;gK]^T: N=128
       constexpr uint32_t id_w = idesc_bf16(128, D, false, true);    // W: N=D, B MN-major
       const uint32_t q_s = sb + C::OFF_Q, gq_s = sb + C::OFF_GQ;
       const uint32_t p_s = sb + C::OFF_P, pg_s = sb + C::OFF_PG;
       bool ok = wait_bar(q_full, 0, abort_flag, prm.status);
-      auto issue_w = [&](int t) {
-        const uint32_t st = sb + C::OFF_ST + (t % C::STAGES) * C::SB;
-        const uint32_t v_s = st + 2 * C::KB, gv_s = st + 3 * C::KB;
+      auto issue_w = [&](int t) -> bool {
+        const int s = t % C::STAGES;
+        if (!wait_bar(v_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
+        tc_fence_after();
+        const uint32_t st = sb + C::OFF_V + s * C::SB;
+        const uint32_t v_s = st, gv_s = st + C::KB;
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 keys
           mma_bf16(tmem + C::T_W, desc_kmajor(p_s + k * 32), desc_mnmajor(gv_s + k * 2048, C::BN * 128),
@@ -257,35 +295,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                    id_w, 1u);
         }
         mma_commit(p_empty);
-        mma_commit(kv_empty + (t % C::STAGES));
+        mma_commit(v_empty + s);
+        return true;
       };
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES, b = t & 1;
-        if (!wait_bar(kv_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (!wait_bar(kg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
         if (t >= 2 && !wait_bar(sg_empty + b, ((t >> 1) - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t st = sb + C::OFF_ST + s * C::SB;
-        const uint32_t k_s = st, gk_s = st + C::KB;
+        const uint32_t kgk_s = sb + C::OFF_KG + s * C::SB;  // [K;gK] per box, 2*BN rows
+        // [S | Q gK^T] = Q [K; gK]^T in one N=128 MMA chain (T_G(b) = T_S(b) + 64)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_S(b), kslice(q_s, C::BM, k), kslice(k_s, C::BN, k), id_s, k > 0);
+          mma_bf16(tmem + C::T_S(b), kslice(q_s, C::BM, k), kslice(kgk_s, 2 * C::BN, k), id_sg,
+                   k > 0);
+        // G += gQ K^T (the first BN rows of each [K;gK] box are K)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_G(b), kslice(q_s, C::BM, k), kslice(gk_s, C::BN, k), id_s, k > 0);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_G(b), kslice(gq_s, C::BM, k), kslice(k_s, C::BN, k), id_s, 1u);
+          mma_bf16(tmem + C::T_G(b), kslice(gq_s, C::BM, k), kslice(kgk_s, 2 * C::BN, k), id_s, 1u);
         mma_commit(sg_full + b);
+        mma_commit(kg_empty + s);
         if (t >= 1) {
           if (!wait_bar(p_full, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
           tc_fence_after();
-          issue_w(t - 1);
+          if (!issue_w(t - 1)) { ok = false; break; }
         }
       }
       if (ok && wait_bar(p_full, (T - 1) & 1, abort_flag, prm.status)) {
         tc_fence_after();
-        issue_w(T - 1);
-        mma_commit(w_done);
+        if (issue_w(T - 1)) mma_commit(w_done);
       }
       // every MMA this thread issued has completed before TMEM is released
       mma_commit(drain);
@@ -308,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(sg_full + b, (t >> 1) & 1, abort_flag, prm.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[32], gr[32];
-      tmem_ld32(tmem + lane_off + C::T_S(b) + 32 * half, sr);
-      tmem_ld32(tmem + lane_off + C::T_G(b) + 32 * half, gr);
+      tmem_ld32x2(tmem + lane_off + C::T_S(b) + 32 * half, tmem + lane_off + C::T_G(b) + 32 * half,
+                  sr, gr);
       tc_fence_before();
       mbar_arrive(sg_empty + b);
       const int j0 = t * C::BN + 32 * half;
@@ -317,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pw[16], pgw[16];
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
-        float p0 = exp2f(__uint_as_float(sr[c]) * sc2 - lse2);
-        float p1 = exp2f(__uint_as_float(sr[c + 1]) * sc2 - lse2);
+        float p0 = ex2_approx(__uint_as_float(sr[c]) * sc2 - lse2);
+        float p1 = ex2_approx(__uint_as_float(sr[c + 1]) * sc2 - lse2);
         if (need_mask) {
           const int j = j0 + c;
           if (!(row_ok && j < N && (!prm.causal || j <= i))) p0 = 0.f;
@@ -330,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         pw[c >> 1] = pack_bf16(p0, p1);
         pgw[c >> 1] = pack_bf16(g0, g1);
       }
+      keep16(pw);  // finish the elementwise work before waiting for the P buffer
+      keep16(pgw);
       if (t >= 1 && !warp_wait(p_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
       store_row_chunk(sb + C::OFF_P, row, 4 * half, pw);
       store_row_chunk(sb + C::OFF_PG, row, 4 * half, pgw);
@@ -423,9 +463,12 @@ struct Col {
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "pass 2 shared memory budget");
   // TMEM columns
-  static constexpr uint32_t T_S = 0, T_DP = 64, T_G = 128, T_H = 192, T_GK = 256, T_GV = 256 + D;
-  static constexpr bool GQ_IN_H = (256 + 2 * D + 64 > 512);
-  static constexpr uint32_t T_GQ = GQ_IN_H ? T_H : 256 + 2 * D;
+  // S^T and G^T adjacent: one N=128 MMA chain writes [S^T | K gQ^T]
+  static constexpr uint32_t T_S = 0, T_G = 64, T_DP = 128, T_H = 192, T_GK = 256, T_GV = 256 + D;
+  // gradQ^T partial (64 columns): its own region when TMEM has room (d = 64),
+  // else the S^T columns, which the next tile rewrites last (d = 128)
+  static constexpr bool GQ_IN_S = (256 + 2 * D + 64 > 512);
+  static constexpr uint32_t T_GQ = GQ_IN_S ? T_S : 256 + 2 * D;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -456,10 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC);
+  // stage = [Q|gQ] + scalars (qg_*) and dO (do_*), released separately
   uint64_t* kv_full = bars + 0;
-  uint64_t* st_full = bars + 1;                 // [STAGES]
-  uint64_t* st_empty = bars + 1 + C::STAGES;    // [STAGES]  (MMA commit + consumers)
-  uint64_t* sc_full = bars + 1 + 2 * C::STAGES;
+  uint64_t* qg_full = bars + 1;                 // [STAGES]
+  uint64_t* qg_empty = qg_full + C::STAGES;     // [STAGES] (MMA commit + consumers)
+  uint64_t* do_full = qg_empty + C::STAGES;     // [STAGES]
+  uint64_t* do_empty = do_full + C::STAGES;     // [STAGES]
+  uint64_t* sc_full = do_empty + C::STAGES;
   uint64_t* sc_empty = sc_full + 1;
   uint64_t* ds_full = sc_empty + 1;
   uint64_t* gq_full = ds_full + 1;
@@ -480,8 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(st_full + s, 1);
-      mbar_init(st_empty + s, 1 + kConsumers);
+      mbar_init(qg_full + s, 1);
+      mbar_init(qg_empty + s, 1 + kConsumers);
+      mbar_init(do_full + s, 1);
+      mbar_init(do_empty + s, 1);
     }
     mbar_init(sc_full, 1);
     mbar_init(sc_empty, kConsumers);
@@ -514,48 +562,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     bool ok = true;
+    // row scalars (lse pre-scaled by log2 e, D, r, sigma) of the next query
+    // tile are fetched into registers one tile ahead, off the critical path
+    constexpr int PER = C::BN / 32;
+    float pre[4][PER];
+    auto fetch = [&](int q0) {
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int q = q0 + lane + 32 * u;
+        const bool in = q < N;
+        const size_t idx = (size_t)bh * N + (in ? q : 0);
+        pre[0][u] = in ? prm.lse[idx] * kLog2e : 0.f;
+        pre[1][u] = in ? prm.Dv[idx] : 0.f;
+        pre[2][u] = in ? prm.r[idx] : 0.f;
+        pre[3][u] = in ? prm.sigma[idx] : 0.f;
+      }
+    };
+    fetch(qstart);
+    int qg_issued = 0, do_issued = 0;
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
       const int q0 = qstart + t * C::BN;
-      if (t >= C::STAGES) {
-        bool w = true;
-        if (lane == 0) w = wait_bar(st_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status);
-        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-        if (!ok) break;
+      uint8_t* st = smem + C::OFF_ST + s * C::SB;
+      // dO first: the gradV MMA that last reads it finishes earliest
+      bool w = true;
+      if (lane == 0) {
+        if (t >= C::STAGES)
+          w = wait_bar(do_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status);
+        if (w) {
+          mbar_arrive_expect_tx(do_full + s, C::QB);
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_3d(st + 2 * C::QB + b * C::BN * 128, &mDO, do_full + s, 64 * b, q0, bh);
+          ++do_issued;
+        }
+        if (w && t >= C::STAGES)
+          w = wait_bar(qg_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status);
       }
-      // row scalars of this query tile (lse pre-scaled by log2 e)
+      ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (!ok) break;
       float* sc = scal + s * 4 * C::BN;
-      for (int e = lane; e < C::BN; e += 32) {
-        const int q = q0 + e;
-        const bool in = q < N;
-        const size_t idx = (size_t)bh * N + (in ? q : 0);
-        sc[e] = in ? prm.lse[idx] * kLog2e : 0.f;
-        sc[C::BN + e] = in ? prm.Dv[idx] : 0.f;
-        sc[2 * C::BN + e] = in ? prm.r[idx] : 0.f;
-        sc[3 * C::BN + e] = in ? prm.sigma[idx] : 0.f;
-      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = pre[a][u];
       __syncwarp();
       if (lane == 0) {
-        uint8_t* st = smem + C::OFF_ST + s * C::SB;
-        mbar_arrive_expect_tx(st_full + s, C::SB);
+        // [Q|gQ] interleaved per 64-feature box (128 rows per box)
+        mbar_arrive_expect_tx(qg_full + s, 2 * C::QB);
         for (int b = 0; b < D / 64; ++b) {
           const uint32_t bo = b * C::BN * 128;
-          tma_load_3d(st + 0 * C::QB + bo, &mQ, st_full + s, 64 * b, q0, bh);
-          tma_load_3d(st + 1 * C::QB + bo, &mGQ, st_full + s, 64 * b, q0, bh);
-          tma_load_3d(st + 2 * C::QB + bo, &mDO, st_full + s, 64 * b, q0, bh);
+          tma_load_3d(st + 2 * bo, &mQ, qg_full + s, 64 * b, q0, bh);
+          tma_load_3d(st + 2 * bo + C::BN * 128, &mGQ, qg_full + s, 64 * b, q0, bh);
         }
+        ++qg_issued;
       }
+      if (t + 1 < T) fetch(q0 + C::BN);
     }
     if (lane == 0) {
       wait_bar(kv_full, 0, abort_flag, prm.status);
-      if (*abort_flag)
-        for (int t = max(0, T - C::STAGES); t < T; ++t)
-          mbar_wait_bounded(st_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+      if (*abort_flag) {
+        for (int t = max(0, qg_issued - C::STAGES); t < qg_issued; ++t)
+          mbar_wait_bounded(qg_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
                             100000000ull);
+        for (int t = max(0, do_issued - C::STAGES); t < do_issued; ++t)
+          mbar_wait_bounded(do_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+                            100000000ull);
+      }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t id_sc = idesc_bf16(128, 64, false, false);  // scores: M=128 N=64
+      constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // K [Q;gQ]^T: N=128
       constexpr uint32_t id_out = idesc_bf16(128, D, false, true);   // gradK/V: N=D, B MN
       constexpr uint32_t id_gq = idesc_bf16(D, 64, true, true);      // gradQ^T: M=D, A,B MN
       const uint32_t k_s = sb + C::OFF_K, gk_s = sb + C::OFF_GK, v_s = sb + C::OFF_V,
@@ -565,45 +642,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES;
         const uint32_t st = sb + C::OFF_ST + s * C::SB;
-        const uint32_t q_s = st, gq_s = st + C::QB, do_s = st + 2 * C::QB;
-        if (!wait_bar(st_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+        const uint32_t qgq_s = st, q_s = st, gq_s = st + C::BN * 128, do_s = st + 2 * C::QB;
+        // ---- scores: dP^T and H^T (need dO) first, then S^T, G^T (need Q, gQ) ----
+        if (!wait_bar(do_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
         if (t >= 1 && !wait_bar(sc_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_S, kslice(k_s, C::BM, k), kslice(q_s, C::BN, k), id_sc, k > 0);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_G, kslice(gk_s, C::BM, k), kslice(q_s, C::BN, k), id_sc, k > 0);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_G, kslice(k_s, C::BM, k), kslice(gq_s, C::BN, k), id_sc, 1u);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
           mma_bf16(tmem + C::T_DP, kslice(v_s, C::BM, k), kslice(do_s, C::BN, k), id_sc, k > 0);
-        if (C::GQ_IN_H && t >= 1) {
-          if (!wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
-          tc_fence_after();
-        }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_bf16(tmem + C::T_H, kslice(gv_s, C::BM, k), kslice(do_s, C::BN, k), id_sc, k > 0);
+        if (!wait_bar(qg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (C::GQ_IN_S && t >= 1 &&
+            !wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+        tc_fence_after();
+        // [S^T | K gQ^T] = K [Q; gQ]^T, then G^T += gK Q^T (first BN rows per box)
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + C::T_S, kslice(k_s, C::BM, k), kslice(qgq_s, 2 * C::BN, k), id_sg, k > 0);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16(tmem + C::T_G, kslice(gk_s, C::BM, k), kslice(qgq_s, 2 * C::BN, k), id_sc, 1u);
         mma_commit(sc_full);
         // ---- outputs: wait for dS^T, gdP^T, gS^T in shared memory ----
         if (!wait_bar(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 queries
+        for (int k = 0; k < C::BN / 16; ++k)  // contraction over the 64 queries
+          mma_bf16(tmem + C::T_GV, desc_kmajor(gdp_s + k * 32), desc_mnmajor(do_s + k * 2048, C::BN * 128),
+                   id_out, (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit(do_empty + s);
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k) {
           const uint32_t ko = k * 32, kr = k * 2048;
-          mma_bf16(tmem + C::T_GV, desc_kmajor(gdp_s + ko), desc_mnmajor(do_s + kr, C::BN * 128),
-                   id_out, (t > 0 || k > 0) ? 1u : 0u);
-          mma_bf16(tmem + C::T_GK, desc_kmajor(gs_s + ko), desc_mnmajor(q_s + kr, C::BN * 128),
-                   id_out, (t > 0 || k > 0) ? 1u : 0u);
-          mma_bf16(tmem + C::T_GK, desc_kmajor(ds_s + ko), desc_mnmajor(gq_s + kr, C::BN * 128),
-                   id_out, 1u);
+          mma_bf16(tmem + C::T_GK, desc_kmajor(gs_s + ko),
+                   desc_mnmajor(q_s + kr, 2 * C::BN * 128), id_out, (t > 0 || k > 0) ? 1u : 0u);
+          mma_bf16(tmem + C::T_GK, desc_kmajor(ds_s + ko),
+                   desc_mnmajor(gq_s + kr, 2 * C::BN * 128), id_out, 1u);
         }
-        mma_commit(st_empty + s);
-        if (!C::GQ_IN_H && t >= 1) {
+        mma_commit(qg_empty + s);
+        if (!C::GQ_IN_S && t >= 1) {
           if (!wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
           tc_fence_after();
         }
@@ -635,36 +714,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(sc_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[32], dpr[32], gr[32], hr[32];
-      tmem_ld32(tmem + lane_off + C::T_S + 32 * half, sr);
-      tmem_ld32(tmem + lane_off + C::T_DP + 32 * half, dpr);
-      tmem_ld32(tmem + lane_off + C::T_G + 32 * half, gr);
-      tmem_ld32(tmem + lane_off + C::T_H + 32 * half, hr);
+      const uint32_t tl = tmem + lane_off + 32 * half;
+      tmem_ld32x4(tl + C::T_S, tl + C::T_DP, tl + C::T_G, tl + C::T_H, sr, dpr, gr, hr);
       tc_fence_before();
       mbar_arrive(sc_empty);
-      const float* sc = scal + s * 4 * C::BN + 32 * half;
+      const float4* sc4 = reinterpret_cast<const float4*>(scal + s * 4 * C::BN + 32 * half);
       const int qa = q0 + 32 * half;
       const bool need_mask = (qa + 32 > N) || (j0 + C::BM > N) || (prm.causal && qa < j0 + C::BM);
       uint32_t dsw[16], gdw[16], gsw[16];
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float o_ds[2], o_gd[2], o_gs[2];
+      for (int c4 = 0; c4 < 8; ++c4) {  // 4 query columns per step
+        const float4 L = sc4[c4], Dd = sc4[C::BN / 4 + c4], R = sc4[C::BN / 2 + c4],
+                     Sg = sc4[3 * C::BN / 4 + c4];
+        const float lv[4] = {L.x, L.y, L.z, L.w}, dv[4] = {Dd.x, Dd.y, Dd.z, Dd.w},
+                    rv[4] = {R.x, R.y, R.z, R.w}, sv[4] = {Sg.x, Sg.y, Sg.z, Sg.w};
+        float o_ds[4], o_gd[4], o_gs[4];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int cc = c + e;
-          float p = exp2f(__uint_as_float(sr[cc]) * sc2 - sc[cc]);
+        for (int e = 0; e < 4; ++e) {
+          const int cc = 4 * c4 + e;
+          float p = ex2_approx(__uint_as_float(sr[cc]) * sc2 - lv[e]);
           if (need_mask) {
             const int q = qa + cc;
             if (!(q < N && j < N && (!prm.causal || q >= j))) p = 0.f;
           }
-          const float dpm = __uint_as_float(dpr[cc]) - sc[C::BN + cc];
-          const float gm = __uint_as_float(gr[cc]) * prm.scale - sc[2 * C::BN + cc];
+          const float dpm = __uint_as_float(dpr[cc]) - dv[e];
+          const float gm = fmaf(__uint_as_float(gr[cc]), prm.scale, -rv[e]);
           o_ds[e] = p * dpm;
           o_gd[e] = p * gm;
-          o_gs[e] = p * (__uint_as_float(hr[cc]) + gm * dpm - sc[3 * C::BN + cc]);
+          o_gs[e] = p * (fmaf(gm, dpm, __uint_as_float(hr[cc])) - sv[e]);
         }
-        dsw[c >> 1] = pack_bf16(o_ds[0], o_ds[1]);
-        gdw[c >> 1] = pack_bf16(o_gd[0], o_gd[1]);
-        gsw[c >> 1] = pack_bf16(o_gs[0], o_gs[1]);
+        dsw[2 * c4] = pack_bf16(o_ds[0], o_ds[1]);
+        dsw[2 * c4 + 1] = pack_bf16(o_ds[2], o_ds[3]);
+        gdw[2 * c4] = pack_bf16(o_gd[0], o_gd[1]);
+        gdw[2 * c4 + 1] = pack_bf16(o_gd[2], o_gd[3]);
+        gsw[2 * c4] = pack_bf16(o_gs[0], o_gs[1]);
+        gsw[2 * c4 + 1] = pack_bf16(o_gs[2], o_gs[3]);
       }
       // ds buffers of tile t-1 were released by gq_full(t-1), awaited below
       store_row_chunk(sb + C::OFF_DS, row, 4 * half, dsw);
@@ -672,13 +756,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       store_row_chunk(sb + C::OFF_GS, row, 4 * half, gsw);
       fence_async_smem();
       mbar_arrive(ds_full);
-      mbar_arrive(st_empty + s);  // this thread is done with the stage's scalars
+      mbar_arrive(qg_empty + s);  // this thread is done with the stage's scalars
       // ---- gradQ^T partial: TMEM lane = feature index, column = query ----
       if (!warp_wait(gq_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
       tc_fence_after();
+      uint32_t gq[32];
+      tmem_ld32(tmem + lane_off + C::T_GQ + 32 * half, gq);
+      tc_fence_before();
+      mbar_arrive(gq_empty);  // TMEM region free; the reductions follow
       if (D == 128) {
-        uint32_t gq[32];
-        tmem_ld32(tmem + lane_off + C::T_GQ + 32 * half, gq);
         const int dcol = row;
         float* base = prm.acc + ((size_t)bh * N + qa) * D + dcol;
 #pragma unroll
@@ -687,8 +773,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
         // lanes 32w' + x; the upper 16 lanes of each warp hold nothing.
-        uint32_t gq[32];
-        tmem_ld32(tmem + lane_off + C::T_GQ + 32 * half, gq);
         if (lane < 16) {
           const int dcol = 16 * (warp & 3) + lane;
           float* base = prm.acc + ((size_t)bh * N + qa) * D + dcol;
@@ -697,8 +781,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
         }
       }
-      tc_fence_before();
-      mbar_arrive(gq_empty);
     }
     // ---- epilogue: gradK (scaled), gradV ----
     ok = __all_sync(0xffffffffu, ok);
