@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -89,19 +90,40 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
 
+// Tile visited at step t when a CTA starts its loop at tile `rot` and wraps:
+// CTAs of one head sweep the shared operand tiles out of phase, so the L2
+// serves a tile to a few SMs at a time instead of to all of them at once.
+// Every sum over tiles is order-independent.
+__device__ __forceinline__ int rotated(int t, int rot, int T) {
+  const int u = t + rot;
+  return u >= T ? u - T : u;
+}
+
+// One TMA box per [rows][D] tile: the 4-D tensor view (64 features, rows,
+// D/64 feature halves, heads) lands it as D/64 consecutive [rows][64] blocks.
+__device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, uint64_t* bar, int row,
+                                          int bh) {
+  tma_load_4d(dst, map, bar, 0, row, 0, bh);
+}
+
+// Two [rows][D] tiles A and B interleaved per 64-feature half (A_h, B_h,
+// A_h+1, ...): each half holds 2*rows rows, so one N = 2*rows MMA sees A and B
+// stacked.  Maps with one feature half per box.
+template <int D>
+__device__ __forceinline__ void load_pair(uint8_t* dst, const CUtensorMap* mapA,
+                                          const CUtensorMap* mapB, uint64_t* bar, int rows, int row,
+                                          int bh) {
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) {
+    tma_load_4d(dst + h * 2 * rows * 128, mapA, bar, 0, row, h, bh);
+    tma_load_4d(dst + h * 2 * rows * 128 + rows * 128, mapB, bar, 0, row, h, bh);
+  }
+}
+
 // K-major tile [rows][D] stored as D/64 boxes of [rows][64] (128 B rows,
 // 128-byte swizzle).  Descriptor for the k-th 16-element slice along D.
 __device__ __forceinline__ uint64_t kslice(uint32_t base, int rows, int k) {
   return desc_kmajor(base + (uint32_t)((k >> 2) * rows * 128 + (k & 3) * 32));
-}
-
-// 16 consecutive bf16 (one thread's half-row chunk) -> swizzled smem row.
-__device__ __forceinline__ void store_row_chunk(uint32_t tile, uint32_t row, uint32_t chunk0,
-                                                const uint32_t (&w)[16]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    st_shared_v4(tile + sw128_offset(row, chunk0 + q), w[4 * q], w[4 * q + 1], w[4 * q + 2],
-                 w[4 * q + 3]);
 }
 
 // ===========================================================================
@@ -112,17 +134,17 @@ struct Row {
   static constexpr int BM = 128, BN = 64;
   // Two decoupled rings: [K|gK] (read by the S/G MMAs, freed early) and
   // [V|gV] (read by the W MMAs of the same tile, freed one tile later).
-  static constexpr int STAGES = D == 128 ? 2 : 3;
+  static constexpr int STAGES = D == 128 ? 3 : 4;    // [K|gK] ring
+  static constexpr int VSTAGES = D == 128 ? 2 : 3;   // [V|gV] ring
   static constexpr uint32_t QB = BM * D * 2;        // Q or gQ tile
   static constexpr uint32_t KB = BN * D * 2;        // one streamed key-side tile
-  // [K|gK] stage: interleaved per 64-feature box (128 rows per box, so one
-  // N=128 MMA sees K and gK stacked); [V|gV] stage: V then gV
+  // [K|gK] stage: interleaved per 64-feature half (one N=128 MMA sees K and
+  // gK stacked); [V|gV] stage: V then gV, one box each
   static constexpr uint32_t SB = 2 * KB;
-  static constexpr uint32_t PB = BM * BN * 2;       // P or P*G tile
   static constexpr uint32_t OFF_Q = 0, OFF_GQ = QB, OFF_KG = 2 * QB;
   static constexpr uint32_t OFF_V = OFF_KG + STAGES * SB;
-  static constexpr uint32_t OFF_P = OFF_V + STAGES * SB, OFF_PG = OFF_P + PB;
-  static constexpr uint32_t OFF_MISC = OFF_PG + PB;  // barriers, TMEM slot, abort flag
+  static constexpr uint32_t OFF_PART = OFF_V + VSTAGES * SB;  // epilogue sums [4][128]
+  static constexpr uint32_t OFF_MISC = OFF_PART + 4 * 128 * 4;  // barriers, slot, flag
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "pass 1 shared memory budget");
@@ -131,6 +153,9 @@ struct Row {
   __host__ __device__ static constexpr uint32_t T_S(int b) { return 128u * b; }
   __host__ __device__ static constexpr uint32_t T_G(int b) { return 128u * b + 64u; }
   static constexpr uint32_t T_W = 256, TMEM_COLS = 512;
+  // bf16 P and P*G of tile buffer b (the W MMA's A operands): 32 columns each
+  __host__ __device__ static constexpr uint32_t T_P(int b) { return 384u + 64u * b; }
+  __host__ __device__ static constexpr uint32_t T_PG(int b) { return 384u + 64u * b + 32u; }
 };
 
 struct RowParams {
@@ -164,18 +189,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars + 0;
   uint64_t* kg_full = bars + 1;                  // [STAGES]
   uint64_t* kg_empty = kg_full + C::STAGES;      // [STAGES]
-  uint64_t* v_full = kg_empty + C::STAGES;       // [STAGES]
-  uint64_t* v_empty = v_full + C::STAGES;        // [STAGES]
-  uint64_t* sg_full = v_empty + C::STAGES;       // [2]
+  uint64_t* v_full = kg_empty + C::STAGES;       // [VSTAGES]
+  uint64_t* v_empty = v_full + C::VSTAGES;       // [VSTAGES]
+  uint64_t* sg_full = v_empty + C::VSTAGES;      // [2]
   uint64_t* sg_empty = sg_full + 2;              // [2]
-  uint64_t* p_full = sg_empty + 2;
-  uint64_t* p_empty = p_full + 1;
-  uint64_t* w_done = p_empty + 1;
+  uint64_t* p_full = sg_empty + 2;               // [2]
+  uint64_t* p_empty = p_full + 2;                // [2]
+  uint64_t* w_done = p_empty + 2;
   uint64_t* drain = w_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
-  // epilogue partial sums [4][128] reuse the P tile once the last W MMA is done
-  float* part = reinterpret_cast<float*>(smem + C::OFF_P);
+  float* part = reinterpret_cast<float*>(smem + C::OFF_PART);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = prm.N;
@@ -186,21 +210,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int i0 = blk * C::BM;
   const int kend = prm.causal ? min(N, i0 + C::BM) : N;
   const int T = (kend + C::BN - 1) / C::BN;
+  const int rot = blk % T;  // start tile of this CTA's key loop
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(kg_full + s, 1);
       mbar_init(kg_empty + s, 1);
+    }
+    for (int s = 0; s < C::VSTAGES; ++s) {
       mbar_init(v_full + s, 1);
       mbar_init(v_empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sg_full + b, 1);
       mbar_init(sg_empty + b, kConsumers);
+      mbar_init(p_full + b, kConsumers);
+      mbar_init(p_empty + b, 1);
     }
-    mbar_init(p_full, kConsumers);
-    mbar_init(p_empty, 1);
     mbar_init(w_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -220,10 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mK);
       mbar_arrive_expect_tx(q_full, 2 * C::QB);
-      for (int b = 0; b < D / 64; ++b) {
-        tma_load_3d(smem + C::OFF_Q + b * C::BM * 128, &mQ, q_full, 64 * b, i0, bh);
-        tma_load_3d(smem + C::OFF_GQ + b * C::BM * 128, &mGQ, q_full, 64 * b, i0, bh);
-      }
+      load_tile(smem + C::OFF_Q, &mQ, q_full, i0, bh);
+      load_tile(smem + C::OFF_GQ, &mGQ, q_full, i0, bh);
       // [K|gK] runs one tile ahead of [V|gV]: the S/G MMAs of tile t+1 need
       // only K/gK, which are released as soon as the S/G MMAs of tile t-1 end
       int kg_issued = 0, v_issued = 0;
@@ -234,26 +259,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         uint8_t* st = smem + C::OFF_KG + s * C::SB;
         mbar_arrive_expect_tx(kg_full + s, C::SB);
-        for (int b = 0; b < D / 64; ++b) {
-          const uint32_t bo = b * C::BN * 128;
-          tma_load_3d(st + 2 * bo, &mK, kg_full + s, 64 * b, t * C::BN, bh);
-          tma_load_3d(st + 2 * bo + C::BN * 128, &mGK, kg_full + s, 64 * b, t * C::BN, bh);
-        }
+        const int kt = rotated(t, rot, T) * C::BN;
+        load_pair<D>(st, &mK, &mGK, kg_full + s, C::BN, kt, bh);
         ++kg_issued;
         return true;
       };
       auto load_v = [&](int t) -> bool {
-        const int s = t % C::STAGES;
-        if (t >= C::STAGES &&
-            !wait_bar(v_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status))
+        const int s = t % C::VSTAGES;
+        if (t >= C::VSTAGES &&
+            !wait_bar(v_empty + s, ((t / C::VSTAGES) - 1) & 1, abort_flag, prm.status))
           return false;
         uint8_t* st = smem + C::OFF_V + s * C::SB;
         mbar_arrive_expect_tx(v_full + s, C::SB);
-        for (int b = 0; b < D / 64; ++b) {
-          const uint32_t bo = b * C::BN * 128;
-          tma_load_3d(st + bo, &mV, v_full + s, 64 * b, t * C::BN, bh);
-          tma_load_3d(st + C::KB + bo, &mGV, v_full + s, 64 * b, t * C::BN, bh);
-        }
+        const int kt = rotated(t, rot, T) * C::BN;
+        load_tile(st, &mV, v_full + s, kt, bh);
+        load_tile(st + C::KB, &mGV, v_full + s, kt, bh);
         ++v_issued;
         return true;
       };
@@ -268,33 +288,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = max(0, kg_issued - C::STAGES); t < kg_issued; ++t)
           mbar_wait_bounded(kg_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
                             100000000ull);
-        for (int t = max(0, v_issued - C::STAGES); t < v_issued; ++t)
-          mbar_wait_bounded(v_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+        for (int t = max(0, v_issued - C::VSTAGES); t < v_issued; ++t)
+          mbar_wait_bounded(v_full + (t % C::VSTAGES), (t / C::VSTAGES) & 1, prm.status,
                             100000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);  // gQ K^T: M=128 N=64
+      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);    // gQ K^T: M=128 N=64
       constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // Q [K;gK]^T: N=128
       constexpr uint32_t id_w = idesc_bf16(128, D, false, true);    // W: N=D, B MN-major
       const uint32_t q_s = sb + C::OFF_Q, gq_s = sb + C::OFF_GQ;
-      const uint32_t p_s = sb + C::OFF_P, pg_s = sb + C::OFF_PG;
       bool ok = wait_bar(q_full, 0, abort_flag, prm.status);
+      // W += P gV + (P*G) V for tile t: A operands (bf16 P, P*G) from TMEM
       auto issue_w = [&](int t) -> bool {
-        const int s = t % C::STAGES;
-        if (!wait_bar(v_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
+        const int s = t % C::VSTAGES, b = t & 1;
+        if (!wait_bar(p_full + b, (t >> 1) & 1, abort_flag, prm.status)) return false;
+        if (!wait_bar(v_full + s, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
         const uint32_t st = sb + C::OFF_V + s * C::SB;
         const uint32_t v_s = st, gv_s = st + C::KB;
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 keys
-          mma_bf16(tmem + C::T_W, desc_kmajor(p_s + k * 32), desc_mnmajor(gv_s + k * 2048, C::BN * 128),
-                   id_w, (t > 0 || k > 0) ? 1u : 0u);
-          mma_bf16(tmem + C::T_W, desc_kmajor(pg_s + k * 32), desc_mnmajor(v_s + k * 2048, C::BN * 128),
-                   id_w, 1u);
+          mma_bf16_tmem_a(tmem + C::T_W, tmem + C::T_P(b) + 8 * k,
+                          desc_mnmajor(gv_s + k * 2048, C::BN * 128), id_w,
+                          (t > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_tmem_a(tmem + C::T_W, tmem + C::T_PG(b) + 8 * k,
+                          desc_mnmajor(v_s + k * 2048, C::BN * 128), id_w, 1u);
         }
-        mma_commit(p_empty);
+        mma_commit(p_empty + b);
         mma_commit(v_empty + s);
         return true;
       };
@@ -303,28 +325,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(kg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
         if (t >= 2 && !wait_bar(sg_empty + b, ((t >> 1) - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kgk_s = sb + C::OFF_KG + s * C::SB;  // [K;gK] per box, 2*BN rows
+        const uint32_t kgk_s = sb + C::OFF_KG + s * C::SB;  // [K;gK] per half, 2*BN rows
         // [S | Q gK^T] = Q [K; gK]^T in one N=128 MMA chain (T_G(b) = T_S(b) + 64)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_bf16(tmem + C::T_S(b), kslice(q_s, C::BM, k), kslice(kgk_s, 2 * C::BN, k), id_sg,
                    k > 0);
-        // G += gQ K^T (the first BN rows of each [K;gK] box are K)
+        // G += gQ K^T (the first BN rows of each [K;gK] half are K)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_bf16(tmem + C::T_G(b), kslice(gq_s, C::BM, k), kslice(kgk_s, 2 * C::BN, k), id_s, 1u);
         mma_commit(sg_full + b);
         mma_commit(kg_empty + s);
-        if (t >= 1) {
-          if (!wait_bar(p_full, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
-          tc_fence_after();
-          if (!issue_w(t - 1)) { ok = false; break; }
-        }
+        if (t >= 1 && !issue_w(t - 1)) { ok = false; break; }
       }
-      if (ok && wait_bar(p_full, (T - 1) & 1, abort_flag, prm.status)) {
-        tc_fence_after();
-        if (issue_w(T - 1)) mma_commit(w_done);
-      }
+      if (ok && issue_w(T - 1)) mma_commit(w_done);
       // every MMA this thread issued has completed before TMEM is released
       mma_commit(drain);
       mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
@@ -350,37 +365,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                   sr, gr);
       tc_fence_before();
       mbar_arrive(sg_empty + b);
-      const int j0 = t * C::BN + 32 * half;
+      const int j0 = rotated(t, rot, T) * C::BN + 32 * half;
       const bool need_mask = !row_ok || (j0 + 32 > N) || (prm.causal && j0 + 31 > i0);
       uint32_t pw[16], pgw[16];
+      auto body = [&](auto masked) {
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float p0 = ex2_approx(__uint_as_float(sr[c]) * sc2 - lse2);
-        float p1 = ex2_approx(__uint_as_float(sr[c + 1]) * sc2 - lse2);
-        if (need_mask) {
-          const int j = j0 + c;
-          if (!(row_ok && j < N && (!prm.causal || j <= i))) p0 = 0.f;
-          if (!(row_ok && j + 1 < N && (!prm.causal || j + 1 <= i))) p1 = 0.f;
+        for (int c = 0; c < 32; c += 2) {
+          float p0 = ex2_approx(__uint_as_float(sr[c]) * sc2 - lse2);
+          float p1 = ex2_approx(__uint_as_float(sr[c + 1]) * sc2 - lse2);
+          if (decltype(masked)::value) {
+            const int jj = j0 + c;
+            p0 = (row_ok && jj < N && (!prm.causal || jj <= i)) ? p0 : 0.f;
+            p1 = (row_ok && jj + 1 < N && (!prm.causal || jj + 1 <= i)) ? p1 : 0.f;
+          }
+          const float g0 = p0 * (__uint_as_float(gr[c]) * prm.scale);
+          const float g1 = p1 * (__uint_as_float(gr[c + 1]) * prm.scale);
+          r_acc += g0 + g1;
+          pw[c >> 1] = pack_bf16(p0, p1);
+          pgw[c >> 1] = pack_bf16(g0, g1);
         }
-        const float g0 = p0 * (__uint_as_float(gr[c]) * prm.scale);
-        const float g1 = p1 * (__uint_as_float(gr[c + 1]) * prm.scale);
-        r_acc += g0 + g1;
-        pw[c >> 1] = pack_bf16(p0, p1);
-        pgw[c >> 1] = pack_bf16(g0, g1);
-      }
+      };
+      if (need_mask)
+        body(std::true_type{});
+      else
+        body(std::false_type{});
       keep16(pw);  // finish the elementwise work before waiting for the P buffer
       keep16(pgw);
-      if (t >= 1 && !warp_wait(p_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
-      store_row_chunk(sb + C::OFF_P, row, 4 * half, pw);
-      store_row_chunk(sb + C::OFF_PG, row, 4 * half, pgw);
-      fence_async_smem();
-      mbar_arrive(p_full);
+      // P buffer b was last read by the W MMAs of tile t-2
+      if (t >= 2 && !warp_wait(p_empty + b, ((t >> 1) - 1) & 1, abort_flag, prm.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st16(tmem + lane_off + C::T_P(b) + 16 * half, pw);
+      tmem_st16(tmem + lane_off + C::T_PG(b) + 16 * half, pgw);
+      tc_fence_before();
+      mbar_arrive(p_full + b);
     }
     // ---- epilogue: r, D, sigma, graddO = W - r O ----
     ok = __all_sync(0xffffffffu, ok);
     if (ok) ok = warp_wait(w_done, 0, abort_flag, prm.status);
     tc_fence_after();
-    consumer_sync();  // P is dead for every thread before it is reused
     part[half * 128 + row] = r_acc;
     consumer_sync();
     const float r = part[row] + part[128 + row];
@@ -485,8 +510,18 @@ struct ColParams {
   float scale;
 };
 
+// Pass 2 warp roles: warps 0-15 elementwise (warp w: TMEM lane quadrant w%4,
+// 16-column slice w/4 of the 64-query tile), warp 16 TMA producer, warp 17
+// TMEM allocator and MMA issuer.
+constexpr int kColConsumerWarps = 16;
+constexpr int kColConsumers = kColConsumerWarps * 32;
+constexpr int kColProducerWarp = kColConsumerWarps;
+constexpr int kColMmaWarp = kColConsumerWarps + 1;
+constexpr int kColThreads = (kColConsumerWarps + 2) * 32;
+constexpr int kColCols = 64 / (kColConsumerWarps / 4);  // columns per elementwise thread
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kColThreads, 1)
     bob_col_pass(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mGK,
                  const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mGV,
                  const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mGQ,
@@ -522,26 +557,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int j0 = (int)blockIdx.x * C::BM;  // low key blocks (most query tiles) first
   const int qstart = prm.causal ? (j0 / C::BN) * C::BN : 0;
   const int T = (N - qstart + C::BN - 1) / C::BN;
+  const int rot = (int)blockIdx.x % T;  // start tile of this CTA's query loop
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(qg_full + s, 1);
-      mbar_init(qg_empty + s, 1 + kConsumers);
+      mbar_init(qg_empty + s, 1 + kColConsumers);
       mbar_init(do_full + s, 1);
       mbar_init(do_empty + s, 1);
     }
     mbar_init(sc_full, 1);
-    mbar_init(sc_empty, kConsumers);
-    mbar_init(ds_full, kConsumers);
+    mbar_init(sc_empty, kColConsumers);
+    mbar_init(ds_full, kColConsumers);
     mbar_init(gq_full, 1);
-    mbar_init(gq_empty, kConsumers);
+    mbar_init(gq_empty, kColConsumers);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kColMmaWarp) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -550,16 +586,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kProducerWarp) {
+  if (warp == kColProducerWarp) {
     if (lane == 0) {
       mbar_arrive_expect_tx(kv_full, 4 * C::KB);
-      for (int b = 0; b < D / 64; ++b) {
-        const uint32_t bo = b * C::BM * 128;
-        tma_load_3d(smem + C::OFF_K + bo, &mK, kv_full, 64 * b, j0, bh);
-        tma_load_3d(smem + C::OFF_GK + bo, &mGK, kv_full, 64 * b, j0, bh);
-        tma_load_3d(smem + C::OFF_V + bo, &mV, kv_full, 64 * b, j0, bh);
-        tma_load_3d(smem + C::OFF_GV + bo, &mGV, kv_full, 64 * b, j0, bh);
-      }
+      load_tile(smem + C::OFF_K, &mK, kv_full, j0, bh);
+      load_tile(smem + C::OFF_GK, &mGK, kv_full, j0, bh);
+      load_tile(smem + C::OFF_V, &mV, kv_full, j0, bh);
+      load_tile(smem + C::OFF_GV, &mGV, kv_full, j0, bh);
     }
     bool ok = true;
     // row scalars (lse pre-scaled by log2 e, D, r, sigma) of the next query
@@ -578,11 +611,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         pre[3][u] = in ? prm.sigma[idx] : 0.f;
       }
     };
-    fetch(qstart);
+    fetch(qstart + rotated(0, rot, T) * C::BN);
     int qg_issued = 0, do_issued = 0;
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
-      const int q0 = qstart + t * C::BN;
+      const int q0 = qstart + rotated(t, rot, T) * C::BN;
+      const int q_next = qstart + rotated(t + 1 < T ? t + 1 : 0, rot, T) * C::BN;
       uint8_t* st = smem + C::OFF_ST + s * C::SB;
       // dO first: the gradV MMA that last reads it finishes earliest
       bool w = true;
@@ -591,8 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           w = wait_bar(do_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status);
         if (w) {
           mbar_arrive_expect_tx(do_full + s, C::QB);
-          for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(st + 2 * C::QB + b * C::BN * 128, &mDO, do_full + s, 64 * b, q0, bh);
+          load_tile(st + 2 * C::QB, &mDO, do_full + s, q0, bh);
           ++do_issued;
         }
         if (w && t >= C::STAGES)
@@ -607,16 +640,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = pre[a][u];
       __syncwarp();
       if (lane == 0) {
-        // [Q|gQ] interleaved per 64-feature box (128 rows per box)
         mbar_arrive_expect_tx(qg_full + s, 2 * C::QB);
-        for (int b = 0; b < D / 64; ++b) {
-          const uint32_t bo = b * C::BN * 128;
-          tma_load_3d(st + 2 * bo, &mQ, qg_full + s, 64 * b, q0, bh);
-          tma_load_3d(st + 2 * bo + C::BN * 128, &mGQ, qg_full + s, 64 * b, q0, bh);
-        }
+        load_pair<D>(st, &mQ, &mGQ, qg_full + s, C::BN, q0, bh);
         ++qg_issued;
+        if (t + 1 < T) {  // warm L2 with the next query tile
+          tma_prefetch_l2_4d(&mQ, 0, q_next, 0, bh);
+          tma_prefetch_l2_4d(&mGQ, 0, q_next, 0, bh);
+          tma_prefetch_l2_4d(&mDO, 0, q_next, 0, bh);
+        }
       }
-      if (t + 1 < T) fetch(q0 + C::BN);
+      if (t + 1 < T) fetch(q_next);
     }
     if (lane == 0) {
       wait_bar(kv_full, 0, abort_flag, prm.status);
@@ -629,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             100000000ull);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kColMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t id_sc = idesc_bf16(128, 64, false, false);  // scores: M=128 N=64
       constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // K [Q;gQ]^T: N=128
@@ -642,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES;
         const uint32_t st = sb + C::OFF_ST + s * C::SB;
+        // [Q;gQ] interleaved per feature half (2*BN rows per half), then dO
         const uint32_t qgq_s = st, q_s = st, gq_s = st + C::BN * 128, do_s = st + 2 * C::QB;
         // ---- scores: dP^T and H^T (need dO) first, then S^T, G^T (need Q, gQ) ----
         if (!wait_bar(do_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
@@ -657,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (C::GQ_IN_S && t >= 1 &&
             !wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
-        // [S^T | K gQ^T] = K [Q; gQ]^T, then G^T += gK Q^T (first BN rows per box)
+        // [S^T | K gQ^T] = K [Q; gQ]^T, then G^T += gK Q^T (first BN rows per half)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_bf16(tmem + C::T_S, kslice(k_s, C::BM, k), kslice(qgq_s, 2 * C::BN, k), id_sg, k > 0);
@@ -702,73 +736,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- elementwise warps: thread = key row -----------------
+    constexpr int NC = kColCols;           // query columns per thread
     const int row = 32 * (warp & 3) + lane;
-    const int half = warp >> 2;
+    const int slice = warp >> 2;           // columns [NC*slice, NC*slice + NC)
     const int j = j0 + row;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sc2 = prm.scale * kLog2e;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
-      const int q0 = qstart + t * C::BN;
+      const int q0 = qstart + rotated(t, rot, T) * C::BN;
       if (!warp_wait(sc_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+      // the stage's row scalars were published with qg_full (already complete)
+      if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[32], dpr[32], gr[32], hr[32];
-      const uint32_t tl = tmem + lane_off + 32 * half;
-      tmem_ld32x4(tl + C::T_S, tl + C::T_DP, tl + C::T_G, tl + C::T_H, sr, dpr, gr, hr);
+      uint32_t sr[NC], dpr[NC], gr[NC], hr[NC];
+      const uint32_t tl = tmem + lane_off + NC * slice;
+      tmem_ld16x4(tl + C::T_S, tl + C::T_DP, tl + C::T_G, tl + C::T_H, sr, dpr, gr, hr);
       tc_fence_before();
       mbar_arrive(sc_empty);
-      const float4* sc4 = reinterpret_cast<const float4*>(scal + s * 4 * C::BN + 32 * half);
-      const int qa = q0 + 32 * half;
-      const bool need_mask = (qa + 32 > N) || (j0 + C::BM > N) || (prm.causal && qa < j0 + C::BM);
-      uint32_t dsw[16], gdw[16], gsw[16];
+      const float4* sc4 = reinterpret_cast<const float4*>(scal + s * 4 * C::BN + NC * slice);
+      const int qa = q0 + NC * slice;
+      const bool need_mask = (qa + NC > N) || (j0 + C::BM > N) || (prm.causal && qa < j0 + C::BM);
+      uint32_t dsw[NC / 2], gdw[NC / 2], gsw[NC / 2];
+      // one body per mask case, so the unmasked bulk carries no per-element
+      // branches
+      auto body = [&](auto masked) {
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {  // 4 query columns per step
-        const float4 L = sc4[c4], Dd = sc4[C::BN / 4 + c4], R = sc4[C::BN / 2 + c4],
-                     Sg = sc4[3 * C::BN / 4 + c4];
-        const float lv[4] = {L.x, L.y, L.z, L.w}, dv[4] = {Dd.x, Dd.y, Dd.z, Dd.w},
-                    rv[4] = {R.x, R.y, R.z, R.w}, sv[4] = {Sg.x, Sg.y, Sg.z, Sg.w};
-        float o_ds[4], o_gd[4], o_gs[4];
+        for (int c4 = 0; c4 < NC / 4; ++c4) {  // 4 query columns per step
+          const float4 L = sc4[c4], Dd = sc4[C::BN / 4 + c4], R = sc4[C::BN / 2 + c4],
+                       Sg = sc4[3 * C::BN / 4 + c4];
+          const float lv[4] = {L.x, L.y, L.z, L.w}, dv[4] = {Dd.x, Dd.y, Dd.z, Dd.w},
+                      rv[4] = {R.x, R.y, R.z, R.w}, sv[4] = {Sg.x, Sg.y, Sg.z, Sg.w};
+          float o_ds[4], o_gd[4], o_gs[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cc = 4 * c4 + e;
-          float p = ex2_approx(__uint_as_float(sr[cc]) * sc2 - lv[e]);
-          if (need_mask) {
-            const int q = qa + cc;
-            if (!(q < N && j < N && (!prm.causal || q >= j))) p = 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const int cc = 4 * c4 + e;
+            float p = ex2_approx(__uint_as_float(sr[cc]) * sc2 - lv[e]);
+            if (decltype(masked)::value) {
+              const int q = qa + cc;
+              p = (q < N && j < N && (!prm.causal || q >= j)) ? p : 0.f;
+            }
+            const float dpm = __uint_as_float(dpr[cc]) - dv[e];
+            const float gm = fmaf(__uint_as_float(gr[cc]), prm.scale, -rv[e]);
+            o_ds[e] = p * dpm;
+            o_gd[e] = p * gm;
+            o_gs[e] = p * (fmaf(gm, dpm, __uint_as_float(hr[cc])) - sv[e]);
           }
-          const float dpm = __uint_as_float(dpr[cc]) - dv[e];
-          const float gm = fmaf(__uint_as_float(gr[cc]), prm.scale, -rv[e]);
-          o_ds[e] = p * dpm;
-          o_gd[e] = p * gm;
-          o_gs[e] = p * (fmaf(gm, dpm, __uint_as_float(hr[cc])) - sv[e]);
+          dsw[2 * c4] = pack_bf16(o_ds[0], o_ds[1]);
+          dsw[2 * c4 + 1] = pack_bf16(o_ds[2], o_ds[3]);
+          gdw[2 * c4] = pack_bf16(o_gd[0], o_gd[1]);
+          gdw[2 * c4 + 1] = pack_bf16(o_gd[2], o_gd[3]);
+          gsw[2 * c4] = pack_bf16(o_gs[0], o_gs[1]);
+          gsw[2 * c4 + 1] = pack_bf16(o_gs[2], o_gs[3]);
         }
-        dsw[2 * c4] = pack_bf16(o_ds[0], o_ds[1]);
-        dsw[2 * c4 + 1] = pack_bf16(o_ds[2], o_ds[3]);
-        gdw[2 * c4] = pack_bf16(o_gd[0], o_gd[1]);
-        gdw[2 * c4 + 1] = pack_bf16(o_gd[2], o_gd[3]);
-        gsw[2 * c4] = pack_bf16(o_gs[0], o_gs[1]);
-        gsw[2 * c4 + 1] = pack_bf16(o_gs[2], o_gs[3]);
+      };
+      if (need_mask)
+        body(std::true_type{});
+      else
+        body(std::false_type{});
+      // ds buffers of tile t-1 were released by gq_full(t-1), awaited below;
+      // this thread's columns are 16-byte chunks [NC*slice/8, +NC/8) of its row
+#pragma unroll
+      for (int q = 0; q < NC / 8; ++q) {
+        const uint32_t chunk = (NC / 8) * slice + q;
+        st_shared_v4(sb + C::OFF_DS + sw128_offset(row, chunk), dsw[4 * q], dsw[4 * q + 1],
+                     dsw[4 * q + 2], dsw[4 * q + 3]);
+        st_shared_v4(sb + C::OFF_GDP + sw128_offset(row, chunk), gdw[4 * q], gdw[4 * q + 1],
+                     gdw[4 * q + 2], gdw[4 * q + 3]);
+        st_shared_v4(sb + C::OFF_GS + sw128_offset(row, chunk), gsw[4 * q], gsw[4 * q + 1],
+                     gsw[4 * q + 2], gsw[4 * q + 3]);
       }
-      // ds buffers of tile t-1 were released by gq_full(t-1), awaited below
-      store_row_chunk(sb + C::OFF_DS, row, 4 * half, dsw);
-      store_row_chunk(sb + C::OFF_GDP, row, 4 * half, gdw);
-      store_row_chunk(sb + C::OFF_GS, row, 4 * half, gsw);
       fence_async_smem();
       mbar_arrive(ds_full);
       mbar_arrive(qg_empty + s);  // this thread is done with the stage's scalars
       // ---- gradQ^T partial: TMEM lane = feature index, column = query ----
       if (!warp_wait(gq_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
       tc_fence_after();
-      uint32_t gq[32];
-      tmem_ld32(tmem + lane_off + C::T_GQ + 32 * half, gq);
+      uint32_t gq[NC];
+      tmem_ld16(tmem + lane_off + C::T_GQ + NC * slice, gq);
       tc_fence_before();
       mbar_arrive(gq_empty);  // TMEM region free; the reductions follow
       if (D == 128) {
         const int dcol = row;
         float* base = prm.acc + ((size_t)bh * N + qa) * D + dcol;
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
+        for (int c = 0; c < NC; ++c)
           if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
       } else {
         // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
@@ -777,30 +830,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int dcol = 16 * (warp & 3) + lane;
           float* base = prm.acc + ((size_t)bh * N + qa) * D + dcol;
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
+          for (int c = 0; c < NC; ++c)
             if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
         }
       }
     }
-    // ---- epilogue: gradK (scaled), gradV ----
+    // ---- epilogue: gradK (scaled), gradV; each thread D/4 features ----
     ok = __all_sync(0xffffffffu, ok);
     if (ok) ok = warp_wait(acc_done, 0, abort_flag, prm.status);
     tc_fence_after();
     if (ok) {  // warp-uniform: every lane loads TMEM, rows past N do not store
-      constexpr int HALF = D / 2;
+      constexpr int PART = D / 4;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         __nv_bfloat16* out = which == 0 ? prm.gradk : prm.gradv;
         const float mul = which == 0 ? prm.scale : 1.f;
-        const uint32_t tcol = (which == 0 ? C::T_GK : C::T_GV) + HALF * half;
-        uint4* op = reinterpret_cast<uint4*>(out + ((size_t)bh * N + j) * D + HALF * half);
+        const uint32_t tcol = (which == 0 ? C::T_GK : C::T_GV) + PART * slice;
+        uint4* op = reinterpret_cast<uint4*>(out + ((size_t)bh * N + j) * D + PART * slice);
 #pragma unroll
-        for (int cc = 0; cc < HALF; cc += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + tcol + cc, v);
+        for (int cc = 0; cc < PART; cc += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_off + tcol + cc, v);
           if (j < N) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
               uint32_t w4[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e)
@@ -815,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kColMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -849,16 +902,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [B*H, N, D] bf16 tensor, box = 64 features x box_rows rows, 128-byte swizzle;
-// rows past N read as zero.
-bool make_map(CUtensorMap* m, const void* ptr, const Problem& p, int box_rows) {
+// [B*H, N, D] bf16 tensor viewed 4-D as (64 features, N rows, D/64 halves,
+// B*H heads); one box = box_rows rows x all D features, landing in shared
+// memory as D/64 consecutive [box_rows][64] blocks with 128-byte swizzle.
+// Rows past N read as zero.
+// With one_half the box spans a single 64-feature half (for interleaved pairs).
+bool make_map(CUtensorMap* m, const void* ptr, const Problem& p, int box_rows,
+              bool one_half = false) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.N, (cuuint64_t)p.BH()};
-  cuuint64_t strides[2] = {(cuuint64_t)p.d * 2, (cuuint64_t)p.N * p.d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+  cuuint64_t dims[4] = {64, (cuuint64_t)p.N, (cuuint64_t)(p.d / 64), (cuuint64_t)p.BH()};
+  cuuint64_t strides[3] = {(cuuint64_t)p.d * 2, 128, (cuuint64_t)p.N * p.d * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, one_half ? 1u : (cuuint32_t)(p.d / 64), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -872,13 +929,13 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
   using Cc = Col<D>;
   CUtensorMap mQr, mGQr, mKr, mGKr, mVr, mGVr;
   if (!make_map(&mQr, q, p, R::BM) || !make_map(&mGQr, gq, p, R::BM) ||
-      !make_map(&mKr, k, p, R::BN) || !make_map(&mGKr, gk, p, R::BN) ||
+      !make_map(&mKr, k, p, R::BN, true) || !make_map(&mGKr, gk, p, R::BN, true) ||
       !make_map(&mVr, v, p, R::BN) || !make_map(&mGVr, gv, p, R::BN))
     return cudaErrorInvalidValue;
   CUtensorMap mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc;
   if (!make_map(&mKc, k, p, Cc::BM) || !make_map(&mGKc, gk, p, Cc::BM) ||
       !make_map(&mVc, v, p, Cc::BM) || !make_map(&mGVc, gv, p, Cc::BM) ||
-      !make_map(&mQc, q, p, Cc::BN) || !make_map(&mGQc, gq, p, Cc::BN) ||
+      !make_map(&mQc, q, p, Cc::BN, true) || !make_map(&mGQc, gq, p, Cc::BN, true) ||
       !make_map(&mDOc, dO, p, Cc::BN))
     return cudaErrorInvalidValue;
 
@@ -921,7 +978,7 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
   cp.causal = p.causal;
   cp.scale = p.scale;
   dim3 g2((p.N + Cc::BM - 1) / Cc::BM, p.BH());
-  bob_col_pass<D><<<g2, kThreads, Cc::SMEM, log.stream>>>(mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc, cp);
+  bob_col_pass<D><<<g2, kColThreads, Cc::SMEM, log.stream>>>(mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc, cp);
   e = cudaGetLastError();
   log.mark();
   if (e != cudaSuccess) return e;
