@@ -148,14 +148,13 @@ struct Row {
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "pass 1 shared memory budget");
-  // TMEM columns
-  // S and G of tile buffer b at columns 128b and 128b + 64
-  __host__ __device__ static constexpr uint32_t T_S(int b) { return 128u * b; }
-  __host__ __device__ static constexpr uint32_t T_G(int b) { return 128u * b + 64u; }
-  static constexpr uint32_t T_W = 256, TMEM_COLS = 512;
-  // bf16 P and P*G of tile buffer b (the W MMA's A operands): 32 columns each
-  __host__ __device__ static constexpr uint32_t T_P(int b) { return 384u + 64u * b; }
-  __host__ __device__ static constexpr uint32_t T_PG(int b) { return 384u + 64u * b + 32u; }
+  // TMEM columns: S and G (one buffer; the elementwise warps free it right
+  // after loading), W, bf16 P and P*G (two buffers), and the stationary bf16
+  // Q and gQ as MMA A operands (D/2 columns each)
+  static constexpr uint32_t T_S = 0, T_G = 64, T_W = 128, TMEM_COLS = 512;
+  __host__ __device__ static constexpr uint32_t T_P(int b) { return 256u + 64u * b; }
+  __host__ __device__ static constexpr uint32_t T_PG(int b) { return 256u + 64u * b + 32u; }
+  static constexpr uint32_t T_QA = 384, T_GQA = 384 + D / 2;
 };
 
 struct RowParams {
@@ -196,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = sg_empty + 2;               // [2]
   uint64_t* p_empty = p_full + 2;                // [2]
   uint64_t* w_done = p_empty + 2;
+  uint64_t* q_tmem = w_done + 2;                  // Q, gQ copied into TMEM
   uint64_t* drain = w_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(w_done, 1);
     mbar_init(drain, 1);
+    mbar_init(q_tmem, kConsumers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -298,8 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);    // gQ K^T: M=128 N=64
       constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // Q [K;gK]^T: N=128
       constexpr uint32_t id_w = idesc_bf16(128, D, false, true);    // W: N=D, B MN-major
-      const uint32_t q_s = sb + C::OFF_Q, gq_s = sb + C::OFF_GQ;
-      bool ok = wait_bar(q_full, 0, abort_flag, prm.status);
+      bool ok = wait_bar(q_tmem, 0, abort_flag, prm.status);
       // W += P gV + (P*G) V for tile t: A operands (bf16 P, P*G) from TMEM
       auto issue_w = [&](int t) -> bool {
         const int s = t % C::VSTAGES, b = t & 1;
@@ -321,21 +321,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       for (int t = 0; ok && t < T; ++t) {
-        const int s = t % C::STAGES, b = t & 1;
+        const int s = t % C::STAGES;
         if (!wait_bar(kg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
-        if (t >= 2 && !wait_bar(sg_empty + b, ((t >> 1) - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (t >= 1 && !wait_bar(sg_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t kgk_s = sb + C::OFF_KG + s * C::SB;  // [K;gK] per half, 2*BN rows
-        // [S | Q gK^T] = Q [K; gK]^T in one N=128 MMA chain (T_G(b) = T_S(b) + 64)
+        // [S | Q gK^T] = Q [K; gK]^T in one N=128 MMA chain (T_G = T_S + 64),
+        // A = Q from TMEM
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_S(b), kslice(q_s, C::BM, k), kslice(kgk_s, 2 * C::BN, k), id_sg,
-                   k > 0);
-        // G += gQ K^T (the first BN rows of each [K;gK] half are K)
+          mma_bf16_tmem_a(tmem + C::T_S, tmem + C::T_QA + 8 * k, kslice(kgk_s, 2 * C::BN, k),
+                          id_sg, k > 0);
+        // G += gQ K^T (the first BN rows of each [K;gK] half are K), A = gQ from TMEM
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_G(b), kslice(gq_s, C::BM, k), kslice(kgk_s, 2 * C::BN, k), id_s, 1u);
-        mma_commit(sg_full + b);
+          mma_bf16_tmem_a(tmem + C::T_G, tmem + C::T_GQA + 8 * k, kslice(kgk_s, 2 * C::BN, k), id_s,
+                          1u);
+        mma_commit(sg_full);
         mma_commit(kg_empty + s);
         if (t >= 1 && !issue_w(t - 1)) { ok = false; break; }
       }
@@ -355,16 +357,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sc2 = prm.scale * kLog2e;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     float r_acc = 0.f;
-    bool ok = true;
-    for (int t = 0; t < T; ++t) {
+    bool ok = warp_wait(q_full, 0, abort_flag, prm.status);
+    if (ok) {
+      // stationary Q and gQ rows -> TMEM (bf16 pairs, lower half = even
+      // feature): one 64-feature half-row per thread and tensor
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const int h = D == 128 ? half : 0;          // feature half copied
+        if (D == 64 && which != half) continue;     // d = 64: half 0 -> Q, half 1 -> gQ
+        const uint32_t src = sb + (which == 0 ? C::OFF_Q : C::OFF_GQ) + h * C::BM * 128 + row * 128;
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              smem + (src - sb) + ((c ^ (row & 7)) << 4));
+          w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+        }
+        const uint32_t dst = tmem + lane_off + (which == 0 ? C::T_QA : C::T_GQA) + 32 * h;
+        uint32_t lo[16], hi[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) { lo[c] = w[c]; hi[c] = w[16 + c]; }
+        tmem_st16(dst, lo);
+        tmem_st16(dst + 16, hi);
+      }
+      tc_fence_before();
+      mbar_arrive(q_tmem);
+    }
+    for (int t = 0; ok && t < T; ++t) {
       const int b = t & 1;
-      if (!warp_wait(sg_full + b, (t >> 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+      if (!warp_wait(sg_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[32], gr[32];
-      tmem_ld32x2(tmem + lane_off + C::T_S(b) + 32 * half, tmem + lane_off + C::T_G(b) + 32 * half,
-                  sr, gr);
+      tmem_ld32x2(tmem + lane_off + C::T_S + 32 * half, tmem + lane_off + C::T_G + 32 * half, sr,
+                  gr);
       tc_fence_before();
-      mbar_arrive(sg_empty + b);
+      mbar_arrive(sg_empty);
       const int j0 = rotated(t, rot, T) * C::BN + 32 * half;
       const bool need_mask = !row_ok || (j0 + 32 > N) || (prm.causal && j0 + 31 > i0);
       uint32_t pw[16], pgw[16];
