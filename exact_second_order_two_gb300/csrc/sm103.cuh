@@ -87,6 +87,43 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same descriptor split into 32-bit words for cheap issue loops.  Every
+// descriptor here uses SBO = 1024, so the high word is one constant; the low
+// word holds start address >> 4 (bits [0,14)) and LBO >> 4 (bits [16,30)).
+// Shared-memory addresses of a CTA are below 256 KB, so offsetting a
+// descriptor by a byte offset `o` inside shared memory is lo + (o >> 4),
+// which never carries into the LBO field.
+constexpr uint32_t kSdescHi = (uint32_t)(((1024u >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29));
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+
+// tcgen05.mma kind::f16, A and B from shared memory, descriptors given by
+// their low words (high word kSdescHi).
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 ad, {%1, %3};\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(kSdescHi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// tcgen05.mma kind::f16, A from TMEM, B from shared memory (low word).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(kSdescHi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // ---- TMEM <-> registers ----------------------------------------------------
 // 32 lanes x 32 consecutive 32-bit columns; thread t of the warp gets lane
 // (warp's lane base + t), registers r[i] = column (taddr.col + i).  The load
@@ -163,6 +200,22 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Three 8-column stores (32 lanes x 8 words each) and one completion wait.
+__device__ __forceinline__ void tmem_st8x3(uint32_t ta, const uint32_t (&a)[8], uint32_t tb,
+                                           const uint32_t (&b)[8], uint32_t tc,
+                                           const uint32_t (&c)[8]) {
+  __syncwarp();
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%3,%4,%5,%6,%7,%8,%9,%10};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%1], {%11,%12,%13,%14,%15,%16,%17,%18};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%2], {%19,%20,%21,%22,%23,%24,%25,%26};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(ta), "r"(tb), "r"(tc),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+      "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7]),
+      "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(c[5]), "r"(c[6]), "r"(c[7])
       : "memory");
 }
 

@@ -53,12 +53,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // MN-major operand descriptor convention: LBO = stride between 64-element
 // groups along M/N, SBO = stride between 8-row groups along K.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
-  return sdesc_sw128(saddr, 16, 1024);
-}
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr, uint32_t mn_group_stride) {
-  return sdesc_sw128(saddr, mn_group_stride, 1024);
-}
 
 // Bounded wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -121,9 +115,24 @@ __device__ __forceinline__ void load_pair(uint8_t* dst, const CUtensorMap* mapA,
 }
 
 // K-major tile [rows][D] stored as D/64 boxes of [rows][64] (128 B rows,
-// 128-byte swizzle).  Descriptor for the k-th 16-element slice along D.
-__device__ __forceinline__ uint64_t kslice(uint32_t base, int rows, int k) {
-  return desc_kmajor(base + (uint32_t)((k >> 2) * rows * 128 + (k & 3) * 32));
+// 128-byte swizzle): offset of the k-th 16-element slice along D, in
+// descriptor units (16 bytes), to add to the tile's descriptor low word.
+__host__ __device__ constexpr uint32_t kslice_off(int rows, int k) {
+  return (uint32_t)(((k >> 2) * rows * 128 + (k & 3) * 32) >> 4);
+}
+// MN-major operand: the k-th 16-row step along K (16 rows x 128 B).
+__host__ __device__ constexpr uint32_t kstep_off(int k) { return (uint32_t)(k * 2048 >> 4); }
+// A value the compiler must treat as new on every evaluation: keeps
+// `base + constant` descriptor words inside the tile loop (one add each)
+// instead of hoisting every unrolled offset into its own register.
+__device__ __forceinline__ uint32_t opaque(uint32_t x) {
+  asm volatile("" : "+r"(x));
+  return x;
+}
+// Descriptor low words (see sdesc_lo).
+__device__ __forceinline__ uint32_t lo_kmajor(uint32_t saddr) { return sdesc_lo(saddr, 16); }
+__device__ __forceinline__ uint32_t lo_mnmajor(uint32_t saddr, uint32_t mn_group_stride) {
+  return sdesc_lo(saddr, mn_group_stride);
 }
 
 // ===========================================================================
@@ -307,14 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(v_full + s, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
         const uint32_t st = sb + C::OFF_V + s * C::SB;
-        const uint32_t v_s = st, gv_s = st + C::KB;
+        const uint32_t v_lo = lo_mnmajor(st, C::BN * 128), gv_lo = lo_mnmajor(st + C::KB, C::BN * 128);
+        const uint32_t tw = tmem + C::T_W, tp = tmem + C::T_P(b), tpg = tmem + C::T_PG(b);
+        const uint32_t first = t > 0 ? 1u : 0u;
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 keys
-          mma_bf16_tmem_a(tmem + C::T_W, tmem + C::T_P(b) + 8 * k,
-                          desc_mnmajor(gv_s + k * 2048, C::BN * 128), id_w,
-                          (t > 0 || k > 0) ? 1u : 0u);
-          mma_bf16_tmem_a(tmem + C::T_W, tmem + C::T_PG(b) + 8 * k,
-                          desc_mnmajor(v_s + k * 2048, C::BN * 128), id_w, 1u);
+          mma_ts(tw, tp + 8 * k, gv_lo + kstep_off(k), id_w, k > 0 ? 1u : first);
+          mma_ts(tw, tpg + 8 * k, v_lo + kstep_off(k), id_w, 1u);
         }
         mma_commit(p_empty + b);
         mma_commit(v_empty + s);
@@ -325,18 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(kg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
         if (t >= 1 && !wait_bar(sg_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kgk_s = sb + C::OFF_KG + s * C::SB;  // [K;gK] per half, 2*BN rows
+        // [K;gK] per half, 2*BN rows
+        const uint32_t kgk_lo = lo_kmajor(sb + C::OFF_KG + s * C::SB);
+        const uint32_t ts = tmem + C::T_S, tg = tmem + C::T_G, tq = tmem + C::T_QA,
+                       tgq = tmem + C::T_GQA;
         // [S | Q gK^T] = Q [K; gK]^T in one N=128 MMA chain (T_G = T_S + 64),
         // A = Q from TMEM
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16_tmem_a(tmem + C::T_S, tmem + C::T_QA + 8 * k, kslice(kgk_s, 2 * C::BN, k),
-                          id_sg, k > 0);
+          mma_ts(ts, tq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_sg, k > 0 ? 1u : 0u);
         // G += gQ K^T (the first BN rows of each [K;gK] half are K), A = gQ from TMEM
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16_tmem_a(tmem + C::T_G, tmem + C::T_GQA + 8 * k, kslice(kgk_s, 2 * C::BN, k), id_s,
-                          1u);
+          mma_ts(tg, tgq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_s, 1u);
         mma_commit(sg_full);
         mma_commit(kg_empty + s);
         if (t >= 1 && !issue_w(t - 1)) { ok = false; break; }
@@ -500,22 +509,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 struct Col {
   static constexpr int BM = 128, BN = 64;
-  static constexpr int STAGES = D == 128 ? 1 : 2;
+  static constexpr int STAGES = D == 128 ? 1 : 2;    // [Q|gQ] (+ row scalars) ring
+  static constexpr int DSTAGES = 2;                  // dO ring
   static constexpr uint32_t KB = BM * D * 2;     // stationary K, gK, V, gV tile
   static constexpr uint32_t QB = BN * D * 2;     // streamed Q, gQ, dO tile
-  static constexpr uint32_t SB = 3 * QB;
-  static constexpr uint32_t XB = BM * BN * 2;    // dS^T / gdP^T / gS^T tile
+  static constexpr uint32_t XB = BM * BN * 2;    // dS^T / gS^T tile (gradQ^T B operands)
   static constexpr uint32_t OFF_K = 0, OFF_GK = KB, OFF_V = 2 * KB, OFF_GV = 3 * KB;
-  static constexpr uint32_t OFF_ST = 4 * KB;
-  static constexpr uint32_t OFF_DS = OFF_ST + STAGES * SB, OFF_GDP = OFF_DS + XB,
-                            OFF_GS = OFF_GDP + XB;
+  static constexpr uint32_t OFF_QG = 4 * KB;                     // [STAGES][2 * QB]
+  static constexpr uint32_t OFF_DO = OFF_QG + STAGES * 2 * QB;   // [DSTAGES][QB]
+  static constexpr uint32_t OFF_DS = OFF_DO + DSTAGES * QB, OFF_GS = OFF_DS + XB;
   static constexpr uint32_t OFF_SC = OFF_GS + XB;          // [STAGES][4][BN] fp32
   static constexpr uint32_t OFF_MISC = OFF_SC + STAGES * 4 * BN * 4;
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "pass 2 shared memory budget");
   // TMEM columns
-  // S^T and G^T adjacent: one N=128 MMA chain writes [S^T | K gQ^T]
+  // S^T and G^T adjacent: one N=128 MMA chain writes [S^T | K gQ^T].  After
+  // the elementwise warps have read a tile's scores they overwrite, inside
+  // the 16 columns each of them read, G^T with bf16 gS^T, dP^T with bf16
+  // dS^T and H^T with bf16 gdP^T: the A operands of the gradK / gradV MMAs.
   static constexpr uint32_t T_S = 0, T_G = 64, T_DP = 128, T_H = 192, T_GK = 256, T_GV = 256 + D;
   // gradQ^T partial (64 columns): its own region when TMEM has room (d = 64),
   // else the S^T columns, which the next tile rewrites last (d = 128)
@@ -538,14 +550,16 @@ struct ColParams {
 };
 
 // Pass 2 warp roles: warps 0-15 elementwise (warp w: TMEM lane quadrant w%4,
-// 16-column slice w/4 of the 64-query tile), warp 16 TMA producer, warp 17
-// TMEM allocator and MMA issuer.
+// 16-column slice w/4 of the 64-query tile, which is also the 16-query
+// contraction step w/4 of the gradK / gradV MMAs), warp 16 TMA producer,
+// warp 17 TMEM allocator and MMA issuer.
 constexpr int kColConsumerWarps = 16;
 constexpr int kColConsumers = kColConsumerWarps * 32;
 constexpr int kColProducerWarp = kColConsumerWarps;
 constexpr int kColMmaWarp = kColConsumerWarps + 1;
 constexpr int kColThreads = (kColConsumerWarps + 2) * 32;
 constexpr int kColCols = 64 / (kColConsumerWarps / 4);  // columns per elementwise thread
+static_assert(kColCols == 16, "one 16-query MMA step per column slice");
 
 template <int D>
 __global__ void __launch_bounds__(kColThreads, 1)
@@ -561,15 +575,13 @@ __global__ void __launch_bounds__(kColThreads, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC);
-  // stage = [Q|gQ] + scalars (qg_*) and dO (do_*), released separately
   uint64_t* kv_full = bars + 0;
-  uint64_t* qg_full = bars + 1;                 // [STAGES]
-  uint64_t* qg_empty = qg_full + C::STAGES;     // [STAGES] (MMA commit + consumers)
-  uint64_t* do_full = qg_empty + C::STAGES;     // [STAGES]
-  uint64_t* do_empty = do_full + C::STAGES;     // [STAGES]
-  uint64_t* sc_full = do_empty + C::STAGES;
-  uint64_t* sc_empty = sc_full + 1;
-  uint64_t* ds_full = sc_empty + 1;
+  uint64_t* qg_full = bars + 1;                 // [STAGES]: [Q|gQ] landed, scalars written
+  uint64_t* qg_empty = qg_full + C::STAGES;     // [STAGES]: gradK MMAs done with [Q|gQ]
+  uint64_t* do_full = qg_empty + C::STAGES;     // [DSTAGES]
+  uint64_t* do_empty = do_full + C::DSTAGES;    // [DSTAGES]: gradV MMAs done with dO
+  uint64_t* sc_full = do_empty + C::DSTAGES;    // scores in TMEM
+  uint64_t* ds_full = sc_full + 1;              // A operands in TMEM, dS^T / gS^T in smem
   uint64_t* gq_full = ds_full + 1;
   uint64_t* gq_empty = gq_full + 1;
   uint64_t* acc_done = gq_empty + 1;
@@ -590,12 +602,13 @@ __global__ void __launch_bounds__(kColThreads, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(qg_full + s, 1);
-      mbar_init(qg_empty + s, 1 + kColConsumers);
+      mbar_init(qg_empty + s, 1);
+    }
+    for (int s = 0; s < C::DSTAGES; ++s) {
       mbar_init(do_full + s, 1);
       mbar_init(do_empty + s, 1);
     }
     mbar_init(sc_full, 1);
-    mbar_init(sc_empty, kColConsumers);
     mbar_init(ds_full, kColConsumers);
     mbar_init(gq_full, 1);
     mbar_init(gq_empty, kColConsumers);
@@ -641,18 +654,17 @@ __global__ void __launch_bounds__(kColThreads, 1)
     fetch(qstart + rotated(0, rot, T) * C::BN);
     int qg_issued = 0, do_issued = 0;
     for (int t = 0; t < T; ++t) {
-      const int s = t % C::STAGES;
+      const int s = t % C::STAGES, ds = t % C::DSTAGES;
       const int q0 = qstart + rotated(t, rot, T) * C::BN;
       const int q_next = qstart + rotated(t + 1 < T ? t + 1 : 0, rot, T) * C::BN;
-      uint8_t* st = smem + C::OFF_ST + s * C::SB;
-      // dO first: the gradV MMA that last reads it finishes earliest
+      // dO first: its ring is deeper, so it runs ahead of [Q|gQ]
       bool w = true;
       if (lane == 0) {
-        if (t >= C::STAGES)
-          w = wait_bar(do_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status);
+        if (t >= C::DSTAGES)
+          w = wait_bar(do_empty + ds, ((t / C::DSTAGES) - 1) & 1, abort_flag, prm.status);
         if (w) {
-          mbar_arrive_expect_tx(do_full + s, C::QB);
-          load_tile(st + 2 * C::QB, &mDO, do_full + s, q0, bh);
+          mbar_arrive_expect_tx(do_full + ds, C::QB);
+          load_tile(smem + C::OFF_DO + ds * C::QB, &mDO, do_full + ds, q0, bh);
           ++do_issued;
         }
         if (w && t >= C::STAGES)
@@ -660,6 +672,8 @@ __global__ void __launch_bounds__(kColThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       if (!ok) break;
+      // the stage's scalars were last read by the elementwise warps of tile
+      // t - STAGES, which finished before the gradK MMAs that freed the stage
       float* sc = scal + s * 4 * C::BN;
 #pragma unroll
       for (int a = 0; a < 4; ++a)
@@ -668,7 +682,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(qg_full + s, 2 * C::QB);
-        load_pair<D>(st, &mQ, &mGQ, qg_full + s, C::BN, q0, bh);
+        load_pair<D>(smem + C::OFF_QG + s * 2 * C::QB, &mQ, &mGQ, qg_full + s, C::BN, q0, bh);
         ++qg_issued;
         if (t + 1 < T) {  // warm L2 with the next query tile
           tma_prefetch_l2_4d(&mQ, 0, q_next, 0, bh);
@@ -684,8 +698,8 @@ __global__ void __launch_bounds__(kColThreads, 1)
         for (int t = max(0, qg_issued - C::STAGES); t < qg_issued; ++t)
           mbar_wait_bounded(qg_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
                             100000000ull);
-        for (int t = max(0, do_issued - C::STAGES); t < do_issued; ++t)
-          mbar_wait_bounded(do_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+        for (int t = max(0, do_issued - C::DSTAGES); t < do_issued; ++t)
+          mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
                             100000000ull);
       }
     }
@@ -695,67 +709,85 @@ __global__ void __launch_bounds__(kColThreads, 1)
       constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // K [Q;gQ]^T: N=128
       constexpr uint32_t id_out = idesc_bf16(128, D, false, true);   // gradK/V: N=D, B MN
       constexpr uint32_t id_gq = idesc_bf16(D, 64, true, true);      // gradQ^T: M=D, A,B MN
-      const uint32_t k_s = sb + C::OFF_K, gk_s = sb + C::OFF_GK, v_s = sb + C::OFF_V,
-                     gv_s = sb + C::OFF_GV;
-      const uint32_t ds_s = sb + C::OFF_DS, gdp_s = sb + C::OFF_GDP, gs_s = sb + C::OFF_GS;
-      bool ok = wait_bar(kv_full, 0, abort_flag, prm.status);
-      for (int t = 0; ok && t < T; ++t) {
-        const int s = t % C::STAGES;
-        const uint32_t st = sb + C::OFF_ST + s * C::SB;
-        // [Q;gQ] interleaved per feature half (2*BN rows per half), then dO
-        const uint32_t qgq_s = st, q_s = st, gq_s = st + C::BN * 128, do_s = st + 2 * C::QB;
-        // ---- scores: dP^T and H^T (need dO) first, then S^T, G^T (need Q, gQ) ----
-        if (!wait_bar(do_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
-        if (t >= 1 && !wait_bar(sc_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+      // descriptor low words of the stationary tiles: K-major for the score
+      // MMAs, MN-major (64-feature groups BM*128 bytes apart) for gradQ^T
+      const uint32_t k_lo = lo_kmajor(sb + C::OFF_K), gk_lo = lo_kmajor(sb + C::OFF_GK),
+                     v_lo = lo_kmajor(sb + C::OFF_V), gv_lo = lo_kmajor(sb + C::OFF_GV);
+      const uint32_t k_mn = lo_mnmajor(sb + C::OFF_K, C::BM * 128),
+                     gk_mn = lo_mnmajor(sb + C::OFF_GK, C::BM * 128);
+      const uint32_t ds_mn = lo_mnmajor(sb + C::OFF_DS, 1024), gs_mn = lo_mnmajor(sb + C::OFF_GS, 1024);
+      const uint32_t t_s = tmem + C::T_S, t_g = tmem + C::T_G, t_dp = tmem + C::T_DP,
+                     t_h = tmem + C::T_H, t_gk = tmem + C::T_GK, t_gv = tmem + C::T_GV,
+                     t_gq = tmem + C::T_GQ;
+      // scores of tile t: dP^T and H^T (need dO) first, then S^T, G^T (need Q, gQ)
+      auto issue_scores = [&](int t) -> bool {
+        const int s = t % C::STAGES, ds = t % C::DSTAGES;
+        const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
+        const uint32_t qgq_lo = opaque(lo_kmajor(sb + C::OFF_QG + s * 2 * C::QB));  // [Q;gQ] per half
+        const uint32_t v_l = opaque(v_lo), gv_l = opaque(gv_lo), k_l = opaque(k_lo),
+                       gk_l = opaque(gk_lo);
+        if (!wait_bar(do_full + ds, (t / C::DSTAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_DP, kslice(v_s, C::BM, k), kslice(do_s, C::BN, k), id_sc, k > 0);
+          mma_ss(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc, k > 0 ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_H, kslice(gv_s, C::BM, k), kslice(do_s, C::BN, k), id_sc, k > 0);
-        if (!wait_bar(qg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
-        if (C::GQ_IN_S && t >= 1 &&
-            !wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+          mma_ss(t_h, gv_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc, k > 0 ? 1u : 0u);
+        if (!wait_bar(qg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
+        if (C::GQ_IN_S && t >= 1 && !wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status))
+          return false;
         tc_fence_after();
         // [S^T | K gQ^T] = K [Q; gQ]^T, then G^T += gK Q^T (first BN rows per half)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_S, kslice(k_s, C::BM, k), kslice(qgq_s, 2 * C::BN, k), id_sg, k > 0);
+          mma_ss(t_s, k_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_sg,
+                 k > 0 ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_bf16(tmem + C::T_G, kslice(gk_s, C::BM, k), kslice(qgq_s, 2 * C::BN, k), id_sc, 1u);
+          mma_ss(t_g, gk_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_sc, 1u);
         mma_commit(sc_full);
-        // ---- outputs: wait for dS^T, gdP^T, gS^T in shared memory ----
+        return true;
+      };
+      bool ok = wait_bar(kv_full, 0, abort_flag, prm.status) && issue_scores(0);
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t % C::STAGES, ds = t % C::DSTAGES;
+        const uint32_t qgq_s = sb + C::OFF_QG + s * 2 * C::QB;
+        // B operands MN-major: 64-feature groups 2*BN*128 bytes apart in the
+        // interleaved [Q;gQ] stage, BN*128 apart in the dO tile
+        const uint32_t q_mn = opaque(lo_mnmajor(qgq_s, 2 * C::BN * 128)),
+                       gq_mn = opaque(lo_mnmajor(qgq_s + C::BN * 128, 2 * C::BN * 128));
+        const uint32_t do_mn = opaque(lo_mnmajor(sb + C::OFF_DO + ds * C::QB, C::BN * 128));
+        const uint32_t k_m = opaque(k_mn), gk_m = opaque(gk_mn), ds_m = opaque(ds_mn),
+                       gs_m = opaque(gs_mn);
+        const uint32_t first = t > 0 ? 1u : 0u;
+        // ---- outputs: A operands (bf16 gS^T, dS^T, gdP^T) from TMEM ----
         if (!wait_bar(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
+        // gradK first: it releases the [Q|gQ] stage that the next tile waits for
 #pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k)  // contraction over the 64 queries
-          mma_bf16(tmem + C::T_GV, desc_kmajor(gdp_s + k * 32), desc_mnmajor(do_s + k * 2048, C::BN * 128),
-                   id_out, (t > 0 || k > 0) ? 1u : 0u);
-        mma_commit(do_empty + s);
-#pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k) {
-          const uint32_t ko = k * 32, kr = k * 2048;
-          mma_bf16(tmem + C::T_GK, desc_kmajor(gs_s + ko),
-                   desc_mnmajor(q_s + kr, 2 * C::BN * 128), id_out, (t > 0 || k > 0) ? 1u : 0u);
-          mma_bf16(tmem + C::T_GK, desc_kmajor(ds_s + ko),
-                   desc_mnmajor(gq_s + kr, 2 * C::BN * 128), id_out, 1u);
+        for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 queries
+          mma_ts(t_gk, t_g + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+          mma_ts(t_gk, t_dp + 16 * k, gq_mn + kstep_off(k), id_out, 1u);
         }
         mma_commit(qg_empty + s);
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k)
+          mma_ts(t_gv, t_h + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+        mma_commit(do_empty + ds);
         if (!C::GQ_IN_S && t >= 1) {
           if (!wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
           tc_fence_after();
         }
 #pragma unroll
         for (int k = 0; k < C::BM / 16; ++k) {  // contraction over the 128 keys
-          const uint32_t kr = k * 2048;
-          mma_bf16(tmem + C::T_GQ, desc_mnmajor(k_s + kr, C::BM * 128),
-                   desc_mnmajor(gs_s + kr, 1024), id_gq, k > 0);
-          mma_bf16(tmem + C::T_GQ, desc_mnmajor(gk_s + kr, C::BM * 128),
-                   desc_mnmajor(ds_s + kr, 1024), id_gq, 1u);
+          mma_ss(t_gq, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
+          mma_ss(t_gq, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
         }
         mma_commit(gq_full);
+        // the next tile's scores overwrite the A operands read above; MMAs
+        // from one thread run in issue order
+        if (t + 1 < T && !issue_scores(t + 1)) { ok = false; break; }
       }
       if (ok) mma_commit(acc_done);
       mma_commit(drain);
@@ -780,8 +812,6 @@ __global__ void __launch_bounds__(kColThreads, 1)
       uint32_t sr[NC], dpr[NC], gr[NC], hr[NC];
       const uint32_t tl = tmem + lane_off + NC * slice;
       tmem_ld16x4(tl + C::T_S, tl + C::T_DP, tl + C::T_G, tl + C::T_H, sr, dpr, gr, hr);
-      tc_fence_before();
-      mbar_arrive(sc_empty);
       const float4* sc4 = reinterpret_cast<const float4*>(scal + s * 4 * C::BN + NC * slice);
       const int qa = q0 + NC * slice;
       const bool need_mask = (qa + NC > N) || (j0 + C::BM > N) || (prm.causal && qa < j0 + C::BM);
@@ -822,21 +852,24 @@ __global__ void __launch_bounds__(kColThreads, 1)
         body(std::true_type{});
       else
         body(std::false_type{});
-      // ds buffers of tile t-1 were released by gq_full(t-1), awaited below;
-      // this thread's columns are 16-byte chunks [NC*slice/8, +NC/8) of its row
+      // A operands of the gradK / gradV MMAs: bf16 pairs (low half = even
+      // query) in the first 8 of the 16 columns this thread read from G^T,
+      // dP^T and H^T; one 16-query contraction step per slice
+      tmem_st8x3(tl + C::T_G, gsw, tl + C::T_DP, dsw, tl + C::T_H, gdw);
+      // dS^T and gS^T also go to shared memory as the gradQ^T B operands; the
+      // buffers of tile t-1 were released by gq_full(t-1), awaited below.
+      // This thread's columns are 16-byte chunks [NC*slice/8, +NC/8) of its row.
 #pragma unroll
       for (int q = 0; q < NC / 8; ++q) {
         const uint32_t chunk = (NC / 8) * slice + q;
         st_shared_v4(sb + C::OFF_DS + sw128_offset(row, chunk), dsw[4 * q], dsw[4 * q + 1],
                      dsw[4 * q + 2], dsw[4 * q + 3]);
-        st_shared_v4(sb + C::OFF_GDP + sw128_offset(row, chunk), gdw[4 * q], gdw[4 * q + 1],
-                     gdw[4 * q + 2], gdw[4 * q + 3]);
         st_shared_v4(sb + C::OFF_GS + sw128_offset(row, chunk), gsw[4 * q], gsw[4 * q + 1],
                      gsw[4 * q + 2], gsw[4 * q + 3]);
       }
       fence_async_smem();
+      tc_fence_before();
       mbar_arrive(ds_full);
-      mbar_arrive(qg_empty + s);  // this thread is done with the stage's scalars
       // ---- gradQ^T partial: TMEM lane = feature index, column = query ----
       if (!warp_wait(gq_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
       tc_fence_after();
