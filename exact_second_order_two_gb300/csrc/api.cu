@@ -40,9 +40,9 @@ int check_shape(const fbob_shape_t* s, Problem* out) {
 
 // Kernel family for a validated problem.
 int choose_path(int op, const Problem& p) {
-  // the tensor-core family serves BoB; forward and first backward run on
-  // CUDA cores
-  const bool tc = op == FBOB_OP_BOB && tc_supported(p);
+  // the tensor-core family serves bf16 at d = 64 and 128 (all three ops);
+  // everything else runs on CUDA cores
+  const bool tc = tc_supported(p);
   if (g_force_path == FBOB_PATH_SIMT) return FBOB_PATH_SIMT;
   if (g_force_path == FBOB_PATH_TCGEN05) return tc ? FBOB_PATH_TCGEN05 : -1;
   return tc ? FBOB_PATH_TCGEN05 : FBOB_PATH_SIMT;
@@ -169,7 +169,8 @@ int fbob_forward(const fbob_shape_t* shape, const void* q, const void* k,
   if (st != FBOB_OK) return st;
   LaunchLog log{s};
   if (g_event_count > 0) cudaEventRecord(g_events[0], s);
-  cudaError_t e = simt_forward(p, q, k, v, o, lse, log);
+  cudaError_t e = path == FBOB_PATH_TCGEN05 ? tc_forward(p, q, k, v, o, lse, ws, log)
+                                            : simt_forward(p, q, k, v, o, lse, log);
   g_last_launches = log.launches;
   return to_status(e);
 }
@@ -187,7 +188,10 @@ int fbob_backward(const fbob_shape_t* shape, const void* q, const void* k,
   if (st != FBOB_OK) return st;
   LaunchLog log{s};
   if (g_event_count > 0) cudaEventRecord(g_events[0], s);
-  cudaError_t e = simt_backward(p, q, k, v, o, lse, dO, dq, dk, dv, ws, log);
+  cudaError_t e =
+      path == FBOB_PATH_TCGEN05
+          ? tc_backward(p, q, k, v, o, lse, dO, dq, dk, dv, ws, log)
+          : simt_backward(p, q, k, v, o, lse, dO, dq, dk, dv, ws, log);
   g_last_launches = log.launches;
   return to_status(e);
 }

@@ -51,7 +51,17 @@ cudaError_t simt_bob(const Problem& p, const void* q, const void* k,
                      void* graddo, const Workspace& ws, LaunchLog& log);
 
 // ---- tensor-core (tcgen05 / TMEM / TMA) kernels, bf16, d in {64, 128} ----
-bool tc_supported(const Problem& p);  // BoB only
+bool tc_supported(const Problem& p);
+cudaError_t tc_forward(const Problem& p, const void* q, const void* k,
+                       const void* v, void* o, float* lse, const Workspace& ws,
+                       LaunchLog& log);
+cudaError_t tc_backward(const Problem& p, const void* q, const void* k,
+                        const void* v, const void* o, const float* lse,
+                        const void* dO, void* dq, void* dk, void* dv,
+                        const Workspace& ws, LaunchLog& log);
+// fp32 accumulator [elems] -> bf16 output (elems a multiple of 8).
+cudaError_t launch_acc_to_bf16(const float* acc, void* out, size_t elems,
+                               LaunchLog& log);
 cudaError_t tc_bob(const Problem& p, const void* q, const void* k,
                    const void* v, const void* o, const float* lse,
                    const void* dO, const void* gq, const void* gk,

@@ -1,0 +1,848 @@
+// Tensor-core (tcgen05 / TMEM / TMA) kernels for sm_103a: the attention
+// forward and first backward whose outputs the backward-over-backward of
+// FlashBoB ("FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
+// Attention", Abstract) consumes.  With c the scale:
+//   S = c Q K^T,  LSE_i = log sum_j exp(S_ij),  P = exp(S - LSE),  O = P V;
+//   dP = dO V^T,  D_i = dO_i . O_i,  dS = P*(dP - D),
+//   dQ = c dS K,  dK = c dS^T Q,  dV = P^T dO.
+//
+// forward (row-stationary, 128 query rows per CTA, 64-key tiles): two sweeps
+//   over the key tiles.  The first reduces each row's log-sum-exp from S in
+//   TMEM (running max and sum in registers); the second forms the exactly
+//   normalised P = exp(S - LSE) in bf16 into TMEM and accumulates O += P V
+//   there.  O never needs rescaling, at the price of S computed twice.
+// first backward (key-stationary, 128 key rows per CTA, 64-query tiles):
+//   S^T and dP^T into TMEM; bf16 P^T and dS^T written back into TMEM as the
+//   A operands of dV += P^T dO and dK += dS^T Q; dQ^T partial = K^T dS^T
+//   reduced into an fp32 accumulator, then converted.
+//
+// Warp roles as in the BoB kernels: elementwise warps own TMEM lanes, one TMA
+// producer warp, one MMA warp (TMEM allocator, single-thread issuer).  Every
+// wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm103.cuh"
+#include "tc_common.cuh"
+
+namespace fbob {
+
+using namespace sm103;
+using namespace tc;
+
+namespace {
+
+constexpr int kFwdConsumerWarps = 8;
+constexpr int kFwdConsumers = kFwdConsumerWarps * 32;
+constexpr int kFwdProducerWarp = 8;
+constexpr int kFwdMmaWarp = 9;
+constexpr int kFwdThreads = 320;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ===========================================================================
+// Forward: row-stationary, two sweeps over the key tiles.
+// ===========================================================================
+template <int D>
+struct Fwd {
+  static constexpr int BM = 128, BN = 64;
+  static constexpr int KSTAGES = 4, VSTAGES = 3;
+  static constexpr uint32_t QB = BM * D * 2;   // stationary Q tile
+  static constexpr uint32_t KB = BN * D * 2;   // one streamed K or V tile
+  static constexpr uint32_t OFF_Q = 0, OFF_K = QB, OFF_V = OFF_K + KSTAGES * KB;
+  static constexpr uint32_t OFF_PART = OFF_V + VSTAGES * KB;    // [2 halves][m, l][128]
+  static constexpr uint32_t OFF_MISC = OFF_PART + 4 * 128 * 4;  // barriers, slot, flag
+  static constexpr uint32_t MISC = 512;
+  static constexpr uint32_t SMEM = OFF_MISC + MISC;
+  static_assert(SMEM <= 232448, "forward shared memory budget");
+  // TMEM columns: S (two buffers), O, bf16 P (two buffers), bf16 Q as the A
+  // operand of S = Q K^T
+  static constexpr uint32_t T_O = 128, TMEM_COLS = 512;
+  __host__ __device__ static constexpr uint32_t T_S(int b) { return 64u * b; }
+  __host__ __device__ static constexpr uint32_t T_P(int b) { return 128u + D + 32u * b; }
+  static constexpr uint32_t T_QA = 128 + D + 64;
+  static_assert(T_QA + D / 2 <= TMEM_COLS, "forward TMEM budget");
+};
+
+struct FwdParams {
+  __nv_bfloat16* o;
+  float* lse;
+  int* status;
+  int N, causal;
+  float scale;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fwd_row_pass(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                 const __grid_constant__ CUtensorMap mV, FwdParams prm) {
+  using C = Fwd<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {  // 128-byte swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) report_status(prm.status, FBOB_ERR_CUDA);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;                   // [KSTAGES]
+  uint64_t* k_empty = k_full + C::KSTAGES;       // [KSTAGES]
+  uint64_t* v_full = k_empty + C::KSTAGES;       // [VSTAGES]
+  uint64_t* v_empty = v_full + C::VSTAGES;       // [VSTAGES]
+  uint64_t* s_full = v_empty + C::VSTAGES;       // [2]
+  uint64_t* s_empty = s_full + 2;                // [2]
+  uint64_t* p_full = s_empty + 2;                // [2]
+  uint64_t* p_empty = p_full + 2;                // [2]
+  uint64_t* o_done = p_empty + 2;
+  uint64_t* q_tmem = o_done + 1;
+  uint64_t* drain = q_tmem + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
+  float* part = reinterpret_cast<float*>(smem + C::OFF_PART);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = prm.N;
+  const int bh = blockIdx.y;
+  // heavy (late) row blocks first under a causal mask
+  const int nblk = gridDim.x;
+  const int blk = prm.causal ? (nblk - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int i0 = blk * C::BM;
+  const int kend = prm.causal ? min(N, i0 + C::BM) : N;
+  const int T = (kend + C::BN - 1) / C::BN;
+  const int rot = blk % T;
+  const int I = 2 * T;  // sweep 1: iterations [0, T); sweep 2: [T, 2T)
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::KSTAGES; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < C::VSTAGES; ++s) {
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(s_empty + b, kFwdConsumers);
+      mbar_init(p_full + b, kFwdConsumers);
+      mbar_init(p_empty + b, 1);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(q_tmem, kFwdConsumers);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kFwdMmaWarp) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kFwdProducerWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, C::QB);
+      load_tile(smem + C::OFF_Q, &mQ, q_full, i0, bh);
+      int k_issued = 0, v_issued = 0;
+      for (int i = 0; i < I; ++i) {
+        const int s = i % C::KSTAGES;
+        const int kt = rotated(i < T ? i : i - T, rot, T) * C::BN;
+        if (i >= C::KSTAGES &&
+            !wait_bar(k_empty + s, ((i / C::KSTAGES) - 1) & 1, abort_flag, prm.status))
+          break;
+        mbar_arrive_expect_tx(k_full + s, C::KB);
+        load_tile(smem + C::OFF_K + s * C::KB, &mK, k_full + s, kt, bh);
+        ++k_issued;
+        if (i >= T) {
+          const int t = i - T, vs = t % C::VSTAGES;
+          if (t >= C::VSTAGES &&
+              !wait_bar(v_empty + vs, ((t / C::VSTAGES) - 1) & 1, abort_flag, prm.status))
+            break;
+          mbar_arrive_expect_tx(v_full + vs, C::KB);
+          load_tile(smem + C::OFF_V + vs * C::KB, &mV, v_full + vs, kt, bh);
+          ++v_issued;
+        }
+      }
+      // after an abort, loads still in flight must land before the CTA exits
+      if (*abort_flag) {
+        mbar_wait_bounded(q_full, 0, prm.status, 100000000ull);
+        for (int i = max(0, k_issued - C::KSTAGES); i < k_issued; ++i)
+          mbar_wait_bounded(k_full + (i % C::KSTAGES), (i / C::KSTAGES) & 1, prm.status,
+                            100000000ull);
+        for (int t = max(0, v_issued - C::VSTAGES); t < v_issued; ++t)
+          mbar_wait_bounded(v_full + (t % C::VSTAGES), (t / C::VSTAGES) & 1, prm.status,
+                            100000000ull);
+      }
+    }
+  } else if (warp == kFwdMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);  // S = Q K^T: N = 64
+      constexpr uint32_t id_o = idesc_bf16(128, D, false, true);    // O += P V: N = D, B MN
+      const uint32_t t_o = tmem + C::T_O, t_q = tmem + C::T_QA;
+      bool ok = wait_bar(q_tmem, 0, abort_flag, prm.status);
+      // O += P(t) V(t), A = bf16 P from TMEM, contraction over the 64 keys
+      auto issue_pv = [&](int t) -> bool {
+        const int pb = t & 1, vs = t % C::VSTAGES;
+        if (!wait_bar(p_full + pb, (t >> 1) & 1, abort_flag, prm.status)) return false;
+        if (!wait_bar(v_full + vs, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
+        tc_fence_after();
+        const uint32_t v_mn = opaque(lo_mnmajor(sb + C::OFF_V + vs * C::KB, C::BN * 128));
+        const uint32_t t_p = tmem + C::T_P(pb);
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k)
+          mma_ts(t_o, t_p + 8 * k, v_mn + kstep_off(k), id_o, (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit(p_empty + pb);
+        mma_commit(v_empty + vs);
+        return true;
+      };
+      for (int i = 0; ok && i < I; ++i) {
+        const int s = i % C::KSTAGES, b = i & 1;
+        if (!wait_bar(k_full + s, (i / C::KSTAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (i >= 2 && !wait_bar(s_empty + b, ((i >> 1) - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_lo = opaque(lo_kmajor(sb + C::OFF_K + s * C::KB));
+        const uint32_t t_s = tmem + C::T_S(b);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ts(t_s, t_q + 8 * k, k_lo + kslice_off(C::BN, k), id_s, k > 0 ? 1u : 0u);
+        mma_commit(s_full + b);
+        mma_commit(k_empty + s);
+        if (i >= T + 1 && !issue_pv(i - T - 1)) { ok = false; break; }
+      }
+      if (ok && issue_pv(T - 1)) mma_commit(o_done);
+      // every MMA this thread issued has completed before TMEM is released
+      mma_commit(drain);
+      mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
+    }
+  } else {
+    // ---------------- elementwise warps: thread = query row --------------
+    const int row = 32 * (warp & 3) + lane;
+    const int half = warp >> 2;  // columns [32*half, 32*half + 32) of a key tile
+    const int i = i0 + row;
+    const bool row_ok = i < N;
+    const size_t srow = (size_t)bh * N + (row_ok ? i : 0);
+    const float sc2 = prm.scale * kLog2e;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    bool ok = warp_wait(q_full, 0, abort_flag, prm.status);
+    if (ok) {
+      // stationary Q row -> TMEM (bf16 pairs, lower half = even feature): one
+      // 64-feature half-row per thread (d = 64: the first warp group only)
+      if (half < D / 64) {
+        const uint32_t src = C::OFF_Q + half * C::BM * 128 + row * 128;
+        uint32_t lo[16], hi[16];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(smem + src + ((c ^ (row & 7)) << 4));
+          uint32_t* dst = c < 4 ? lo + 4 * c : hi + 4 * (c - 4);
+          dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+        }
+        const uint32_t dst = tmem + lane_off + C::T_QA + 32 * half;
+        tmem_st16(dst, lo);
+        tmem_st16(dst + 16, hi);
+      }
+      tc_fence_before();
+      mbar_arrive(q_tmem);
+    }
+    // log2-domain running max m2 and sum l = sum_j 2^(S_ij c log2 e - m2)
+    float m2 = -INFINITY, l = 0.f;
+    // S of iteration it (sweep 1: it < T, sweep 2: it >= T) into registers;
+    // false if a wait gave up
+    auto load_s = [&](int it, uint32_t (&sr)[32]) -> bool {
+      const int b = it & 1;
+      if (!warp_wait(s_full + b, (it >> 1) & 1, abort_flag, prm.status)) return false;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + C::T_S(b) + 32 * half, sr);
+      tc_fence_before();
+      mbar_arrive(s_empty + b);
+      return true;
+    };
+    for (int t = 0; ok && t < T; ++t) {
+      uint32_t sr[32];
+      if (!load_s(t, sr)) { ok = false; break; }
+      const int j0 = rotated(t, rot, T) * C::BN + 32 * half;
+      const bool need_mask = !row_ok || (j0 + 32 > N) || (prm.causal && j0 + 31 > i);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int j = j0 + c;
+        const bool in = !need_mask || (row_ok && j < N && (!prm.causal || j <= i));
+        mx = in ? fmaxf(mx, __uint_as_float(sr[c]) * sc2) : mx;
+      }
+      if (mx > m2) {
+        l *= ex2_approx(m2 - mx);  // 2^(-inf) = 0 on the first update
+        m2 = mx;
+      }
+      if (m2 > -INFINITY) {
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int j = j0 + c;
+          const bool in = !need_mask || (row_ok && j < N && (!prm.causal || j <= i));
+          const float e = ex2_approx(__uint_as_float(sr[c]) * sc2 - m2);
+          acc += in ? e : 0.f;
+        }
+        l += acc;
+      }
+    }
+    // combine the two column halves of each row (every consumer thread gets
+    // here, also after a failed wait, so the barrier cannot hang)
+    part[half * 128 + row] = m2;
+    part[256 + half * 128 + row] = l;
+    named_sync<kFwdConsumers>(1);
+    float lse2;
+    {
+      const float ma = part[row], mb = part[128 + row];
+      const float M = fmaxf(ma, mb);
+      const float L = (ma > -INFINITY ? part[256 + row] * ex2_approx(ma - M) : 0.f) +
+                      (mb > -INFINITY ? part[384 + row] * ex2_approx(mb - M) : 0.f);
+      lse2 = (M > -INFINITY && L > 0.f) ? M + log2f(L) : 0.f;
+    }
+    for (int t = 0; ok && t < T; ++t) {
+      uint32_t sr[32];
+      if (!load_s(T + t, sr)) { ok = false; break; }
+      const int j0 = rotated(t, rot, T) * C::BN + 32 * half;
+      const bool need_mask = !row_ok || (j0 + 32 > N) || (prm.causal && j0 + 31 > i);
+      uint32_t pw[16];
+      auto body = [&](auto masked) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float p0 = ex2_approx(__uint_as_float(sr[c]) * sc2 - lse2);
+          float p1 = ex2_approx(__uint_as_float(sr[c + 1]) * sc2 - lse2);
+          if (decltype(masked)::value) {
+            const int j = j0 + c;
+            p0 = (row_ok && j < N && (!prm.causal || j <= i)) ? p0 : 0.f;
+            p1 = (row_ok && j + 1 < N && (!prm.causal || j + 1 <= i)) ? p1 : 0.f;
+          }
+          pw[c >> 1] = pack_bf16(p0, p1);
+        }
+      };
+      if (need_mask)
+        body(std::true_type{});
+      else
+        body(std::false_type{});
+      keep16(pw);
+      const int pb = t & 1;
+      // P buffer pb was last read by the O MMAs of tile t-2
+      if (t >= 2 && !warp_wait(p_empty + pb, ((t >> 1) - 1) & 1, abort_flag, prm.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st16(tmem + lane_off + C::T_P(pb) + 16 * half, pw);
+      tc_fence_before();
+      mbar_arrive(p_full + pb);
+    }
+    // ---- epilogue: O (bf16) and LSE (natural log) ----
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) ok = warp_wait(o_done, 0, abort_flag, prm.status);
+    tc_fence_after();
+    if (ok) {
+      constexpr int HALF = D / 2;
+      uint4* op = reinterpret_cast<uint4*>(prm.o + srow * D + HALF * half);
+#pragma unroll
+      for (int cc = 0; cc < HALF; cc += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_off + C::T_O + HALF * half + cc, v);
+        if (row_ok) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            op[cc / 8 + q] = make_uint4(
+                pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+        }
+      }
+      if (half == 0 && row_ok) prm.lse[srow] = lse2 * kLn2;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kFwdMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ===========================================================================
+// First backward: key-stationary.
+// ===========================================================================
+template <int D>
+struct Bwd {
+  static constexpr int BM = 128, BN = 64;
+  static constexpr int STAGES = 2, DSTAGES = 2;  // Q (+ row scalars) ring, dO ring
+  static constexpr uint32_t KB = BM * D * 2;     // stationary K, V tile
+  static constexpr uint32_t QB = BN * D * 2;     // streamed Q, dO tile
+  static constexpr uint32_t XB = BM * BN * 2;    // dS^T tile (dQ^T B operand)
+  static constexpr uint32_t OFF_K = 0, OFF_V = KB, OFF_Q = 2 * KB;
+  static constexpr uint32_t OFF_DO = OFF_Q + STAGES * QB;
+  static constexpr uint32_t OFF_DS = OFF_DO + DSTAGES * QB;
+  static constexpr uint32_t OFF_SC = OFF_DS + XB;            // [STAGES][2][BN] fp32
+  static constexpr uint32_t OFF_MISC = OFF_SC + STAGES * 2 * BN * 4;
+  static constexpr uint32_t MISC = 512;
+  static constexpr uint32_t SMEM = OFF_MISC + MISC;
+  static_assert(SMEM <= 232448, "backward shared memory budget");
+  // TMEM columns.  After the elementwise warps have read a tile's scores they
+  // overwrite, inside the 16 columns each of them read, S^T with bf16 P^T and
+  // dP^T with bf16 dS^T: the A operands of the dV / dK MMAs.
+  static constexpr uint32_t T_S = 0, T_DP = 64, T_DK = 128, T_DV = 128 + D, T_DQ = 128 + 2 * D;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(T_DQ + 64 <= TMEM_COLS, "backward TMEM budget");
+};
+
+struct BwdParams {
+  const float* lse;
+  const float* Dv;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* acc;  // fp32 [B,H,N,D] dQ accumulator
+  int* status;
+  int N, causal;
+  float scale;
+};
+
+constexpr int kBwdConsumerWarps = 16;
+constexpr int kBwdConsumers = kBwdConsumerWarps * 32;
+constexpr int kBwdProducerWarp = kBwdConsumerWarps;
+constexpr int kBwdMmaWarp = kBwdConsumerWarps + 1;
+constexpr int kBwdThreads = (kBwdConsumerWarps + 2) * 32;
+constexpr int kBwdCols = 16;  // query columns per elementwise thread
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_col_pass(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+                 const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mDO,
+                 BwdParams prm) {
+  using C = Bwd<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {
+    if (threadIdx.x == 0) report_status(prm.status, FBOB_ERR_CUDA);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* q_full = bars + 1;                  // [STAGES]: Q landed, scalars written
+  uint64_t* q_empty = q_full + C::STAGES;       // [STAGES]: dK MMAs done with Q
+  uint64_t* do_full = q_empty + C::STAGES;      // [DSTAGES]
+  uint64_t* do_empty = do_full + C::DSTAGES;    // [DSTAGES]: dV MMAs done with dO
+  uint64_t* sc_full = do_empty + C::DSTAGES;
+  uint64_t* ds_full = sc_full + 1;
+  uint64_t* dq_full = ds_full + 1;
+  uint64_t* dq_empty = dq_full + 1;
+  uint64_t* acc_done = dq_empty + 1;
+  uint64_t* drain = acc_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
+  float* scal = reinterpret_cast<float*>(smem + C::OFF_SC);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = prm.N;
+  const int bh = blockIdx.y;
+  const int j0 = (int)blockIdx.x * C::BM;
+  const int qstart = prm.causal ? (j0 / C::BN) * C::BN : 0;
+  const int T = (N - qstart + C::BN - 1) / C::BN;
+  const int rot = (int)blockIdx.x % T;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(q_full + s, 1);
+      mbar_init(q_empty + s, 1);
+    }
+    for (int s = 0; s < C::DSTAGES; ++s) {
+      mbar_init(do_full + s, 1);
+      mbar_init(do_empty + s, 1);
+    }
+    mbar_init(sc_full, 1);
+    mbar_init(ds_full, kBwdConsumers);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, kBwdConsumers);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kBwdMmaWarp) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kBwdProducerWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * C::KB);
+      load_tile(smem + C::OFF_K, &mK, kv_full, j0, bh);
+      load_tile(smem + C::OFF_V, &mV, kv_full, j0, bh);
+    }
+    // row scalars (LSE pre-scaled by log2 e, D) of the next query tile are
+    // fetched into registers one tile ahead
+    constexpr int PER = C::BN / 32;
+    float pre[2][PER];
+    auto fetch = [&](int q0) {
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int q = q0 + lane + 32 * u;
+        const bool in = q < N;
+        const size_t idx = (size_t)bh * N + (in ? q : 0);
+        pre[0][u] = in ? prm.lse[idx] * kLog2e : 0.f;
+        pre[1][u] = in ? prm.Dv[idx] : 0.f;
+      }
+    };
+    fetch(qstart + rotated(0, rot, T) * C::BN);
+    int q_issued = 0, do_issued = 0;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % C::STAGES, ds = t % C::DSTAGES;
+      const int q0 = qstart + rotated(t, rot, T) * C::BN;
+      bool w = true;
+      if (lane == 0) {
+        if (t >= C::DSTAGES)
+          w = wait_bar(do_empty + ds, ((t / C::DSTAGES) - 1) & 1, abort_flag, prm.status);
+        if (w) {
+          mbar_arrive_expect_tx(do_full + ds, C::QB);
+          load_tile(smem + C::OFF_DO + ds * C::QB, &mDO, do_full + ds, q0, bh);
+          ++do_issued;
+        }
+        if (w && t >= C::STAGES)
+          w = wait_bar(q_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status);
+      }
+      if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) break;
+      // the stage's scalars were last read by the elementwise warps of tile
+      // t - STAGES, which finished before the dK MMAs that freed the stage
+      float* sc = scal + s * 2 * C::BN;
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = pre[a][u];
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full + s, C::QB);
+        load_tile(smem + C::OFF_Q + s * C::QB, &mQ, q_full + s, q0, bh);
+        ++q_issued;
+      }
+      if (t + 1 < T) fetch(qstart + rotated(t + 1, rot, T) * C::BN);
+    }
+    if (lane == 0) {
+      wait_bar(kv_full, 0, abort_flag, prm.status);
+      if (*abort_flag) {
+        for (int t = max(0, q_issued - C::STAGES); t < q_issued; ++t)
+          mbar_wait_bounded(q_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+                            100000000ull);
+        for (int t = max(0, do_issued - C::DSTAGES); t < do_issued; ++t)
+          mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
+                            100000000ull);
+      }
+    }
+  } else if (warp == kBwdMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t id_sc = idesc_bf16(128, 64, false, false);  // scores: M=128 N=64
+      constexpr uint32_t id_out = idesc_bf16(128, D, false, true);   // dK/dV: N=D, B MN
+      constexpr uint32_t id_dq = idesc_bf16(D, 64, true, true);      // dQ^T: M=D, A,B MN
+      const uint32_t k_lo = lo_kmajor(sb + C::OFF_K), v_lo = lo_kmajor(sb + C::OFF_V);
+      const uint32_t k_mn = lo_mnmajor(sb + C::OFF_K, C::BM * 128);
+      const uint32_t ds_mn = lo_mnmajor(sb + C::OFF_DS, 1024);
+      const uint32_t t_s = tmem + C::T_S, t_dp = tmem + C::T_DP, t_dk = tmem + C::T_DK,
+                     t_dv = tmem + C::T_DV, t_dq = tmem + C::T_DQ;
+      // scores of tile t: dP^T (needs dO) first, then S^T (needs Q)
+      auto issue_scores = [&](int t) -> bool {
+        const int s = t % C::STAGES, ds = t % C::DSTAGES;
+        const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
+        const uint32_t q_lo = opaque(lo_kmajor(sb + C::OFF_Q + s * C::QB));
+        const uint32_t v_l = opaque(v_lo), k_l = opaque(k_lo);
+        if (!wait_bar(do_full + ds, (t / C::DSTAGES) & 1, abort_flag, prm.status)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
+                 k > 0 ? 1u : 0u);
+        if (!wait_bar(q_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(t_s, k_l + kslice_off(C::BM, k), q_lo + kslice_off(C::BN, k), id_sc,
+                 k > 0 ? 1u : 0u);
+        mma_commit(sc_full);
+        return true;
+      };
+      bool ok = wait_bar(kv_full, 0, abort_flag, prm.status) && issue_scores(0);
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t % C::STAGES, ds = t % C::DSTAGES;
+        const uint32_t q_mn = opaque(lo_mnmajor(sb + C::OFF_Q + s * C::QB, C::BN * 128));
+        const uint32_t do_mn = opaque(lo_mnmajor(sb + C::OFF_DO + ds * C::QB, C::BN * 128));
+        const uint32_t k_m = opaque(k_mn), ds_m = opaque(ds_mn);
+        const uint32_t first = t > 0 ? 1u : 0u;
+        if (!wait_bar(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+        tc_fence_after();
+        // dK += dS^T Q first: it releases the Q stage
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k)
+          mma_ts(t_dk, t_dp + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+        mma_commit(q_empty + s);
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k)
+          mma_ts(t_dv, t_s + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+        mma_commit(do_empty + ds);
+        if (t >= 1) {
+          if (!wait_bar(dq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int k = 0; k < C::BM / 16; ++k)  // contraction over the 128 keys
+          mma_ss(t_dq, k_m + kstep_off(k), ds_m + kstep_off(k), id_dq, k > 0 ? 1u : 0u);
+        mma_commit(dq_full);
+        // the next tile's scores overwrite the A operands read above; MMAs
+        // from one thread run in issue order
+        if (t + 1 < T && !issue_scores(t + 1)) { ok = false; break; }
+      }
+      if (ok) mma_commit(acc_done);
+      mma_commit(drain);
+      mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
+    }
+  } else {
+    // ---------------- elementwise warps: thread = key row -----------------
+    constexpr int NC = kBwdCols;
+    const int row = 32 * (warp & 3) + lane;
+    const int slice = warp >> 2;  // query columns [NC*slice, NC*slice + NC)
+    const int j = j0 + row;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const float sc2 = prm.scale * kLog2e;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % C::STAGES;
+      const int q0 = qstart + rotated(t, rot, T) * C::BN;
+      if (!warp_wait(sc_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+      if (!warp_wait(q_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[NC], dpr[NC];
+      const uint32_t tl = tmem + lane_off + NC * slice;
+      tmem_ld16x2(tl + C::T_S, tl + C::T_DP, sr, dpr);
+      const float4* sc4 = reinterpret_cast<const float4*>(scal + s * 2 * C::BN + NC * slice);
+      const int qa = q0 + NC * slice;
+      const bool need_mask = (qa + NC > N) || (j0 + C::BM > N) || (prm.causal && qa < j0 + C::BM);
+      uint32_t pw[NC / 2], dsw[NC / 2];
+      auto body = [&](auto masked) {
+#pragma unroll
+        for (int c4 = 0; c4 < NC / 4; ++c4) {
+          const float4 L = sc4[c4], Dd = sc4[C::BN / 4 + c4];
+          const float lv[4] = {L.x, L.y, L.z, L.w}, dv[4] = {Dd.x, Dd.y, Dd.z, Dd.w};
+          float o_p[4], o_ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int cc = 4 * c4 + e;
+            float p = ex2_approx(__uint_as_float(sr[cc]) * sc2 - lv[e]);
+            if (decltype(masked)::value) {
+              const int q = qa + cc;
+              p = (q < N && j < N && (!prm.causal || q >= j)) ? p : 0.f;
+            }
+            o_p[e] = p;
+            o_ds[e] = p * (__uint_as_float(dpr[cc]) - dv[e]);
+          }
+          pw[2 * c4] = pack_bf16(o_p[0], o_p[1]);
+          pw[2 * c4 + 1] = pack_bf16(o_p[2], o_p[3]);
+          dsw[2 * c4] = pack_bf16(o_ds[0], o_ds[1]);
+          dsw[2 * c4 + 1] = pack_bf16(o_ds[2], o_ds[3]);
+        }
+      };
+      if (need_mask)
+        body(std::true_type{});
+      else
+        body(std::false_type{});
+      // A operands of the dV / dK MMAs: bf16 pairs (low half = even query) in
+      // the first 8 of the 16 columns this thread read from S^T and dP^T
+      tmem_st8x2(tl + C::T_S, pw, tl + C::T_DP, dsw);
+      // dS^T also goes to shared memory as the dQ^T B operand; the buffer of
+      // tile t-1 was released by dq_full(t-1), awaited below
+#pragma unroll
+      for (int q = 0; q < NC / 8; ++q) {
+        const uint32_t chunk = (NC / 8) * slice + q;
+        st_shared_v4(sb + C::OFF_DS + sw128_offset(row, chunk), dsw[4 * q], dsw[4 * q + 1],
+                     dsw[4 * q + 2], dsw[4 * q + 3]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+      // ---- dQ^T partial: TMEM lane = feature index, column = query ----
+      if (!warp_wait(dq_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t dq[NC];
+      tmem_ld16(tmem + lane_off + C::T_DQ + NC * slice, dq);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      if (D == 128) {
+        float* base = prm.acc + ((size_t)bh * N + qa) * D + row;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(dq[c]) * prm.scale);
+      } else {
+        // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
+        // lanes 32w' + x; the upper 16 lanes of each warp hold nothing
+        if (lane < 16) {
+          float* base = prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane;
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(dq[c]) * prm.scale);
+        }
+      }
+    }
+    // ---- epilogue: dK (scaled), dV; each thread D/4 features ----
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) ok = warp_wait(acc_done, 0, abort_flag, prm.status);
+    tc_fence_after();
+    if (ok) {
+      constexpr int PART = D / 4;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* out = which == 0 ? prm.dk : prm.dv;
+        const float mul = which == 0 ? prm.scale : 1.f;
+        const uint32_t tcol = (which == 0 ? C::T_DK : C::T_DV) + PART * slice;
+        uint4* op = reinterpret_cast<uint4*>(out + ((size_t)bh * N + j) * D + PART * slice);
+#pragma unroll
+        for (int cc = 0; cc < PART; cc += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_off + tcol + cc, v);
+          if (j < N) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w4[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]) * mul,
+                                  __uint_as_float(v[8 * q + 2 * e + 1]) * mul);
+              op[cc / 8 + q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// D_i = dO_i . O_i (fp32) for every row, and the row's fp32 dQ accumulator
+// cleared: D/8 threads per row, 8 bf16 elements each.
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_prep(const uint4* __restrict__ o, const uint4* __restrict__ dO, float* __restrict__ Dout,
+             float4* __restrict__ acc, size_t rows) {
+  constexpr int G = D / 8;  // threads per row (a power of two dividing 32)
+  const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t r = t / G;
+  const int c = (int)(t % G);
+  float s = 0.f;
+  if (r < rows) {
+    const uint4 ov = o[r * G + c], dv = dO[r * G + c];
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 of = __bfloat1622float2(o2[e]);
+      const float2 df = __bfloat1622float2(d2[e]);
+      s = fmaf(of.x, df.x, fmaf(of.y, df.y, s));
+    }
+    acc[(r * G + c) * 2] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[(r * G + c) * 2 + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = G / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (r < rows && c == 0) Dout[r] = s;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+template <int D>
+cudaError_t forward_d(const Problem& p, const void* q, const void* k, const void* v, void* o,
+                      float* lse, const Workspace& ws, LaunchLog& log) {
+  using C = Fwd<D>;
+  CUtensorMap mQ, mK, mV;
+  if (!make_map(&mQ, q, p, C::BM) || !make_map(&mK, k, p, C::BN) || !make_map(&mV, v, p, C::BN))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fwd_row_pass<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  FwdParams fp;
+  fp.o = static_cast<__nv_bfloat16*>(o);
+  fp.lse = lse;
+  fp.status = ws.status;
+  fp.N = p.N;
+  fp.causal = p.causal;
+  fp.scale = p.scale;
+  dim3 grid((p.N + C::BM - 1) / C::BM, p.BH());
+  fwd_row_pass<D><<<grid, kFwdThreads, C::SMEM, log.stream>>>(mQ, mK, mV, fp);
+  e = cudaGetLastError();
+  log.mark();
+  return e;
+}
+
+template <int D>
+cudaError_t backward_d(const Problem& p, const void* q, const void* k, const void* v,
+                       const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                       void* dv, const Workspace& ws, LaunchLog& log) {
+  using C = Bwd<D>;
+  const size_t rows = p.rows();
+  const size_t threads = rows * (D / 8);
+  bwd_prep<D><<<(unsigned)((threads + 255) / 256), 256, 0, log.stream>>>(
+      static_cast<const uint4*>(o), static_cast<const uint4*>(dO), ws.D,
+      reinterpret_cast<float4*>(ws.acc), rows);
+  cudaError_t e = cudaGetLastError();
+  log.mark();
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap mK, mV, mQ, mDO;
+  if (!make_map(&mK, k, p, C::BM) || !make_map(&mV, v, p, C::BM) ||
+      !make_map(&mQ, q, p, C::BN) || !make_map(&mDO, dO, p, C::BN))
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(bwd_col_pass<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  BwdParams bp;
+  bp.lse = lse;
+  bp.Dv = ws.D;
+  bp.dk = static_cast<__nv_bfloat16*>(dk);
+  bp.dv = static_cast<__nv_bfloat16*>(dv);
+  bp.acc = ws.acc;
+  bp.status = ws.status;
+  bp.N = p.N;
+  bp.causal = p.causal;
+  bp.scale = p.scale;
+  dim3 grid((p.N + C::BM - 1) / C::BM, p.BH());
+  bwd_col_pass<D><<<grid, kBwdThreads, C::SMEM, log.stream>>>(mK, mV, mQ, mDO, bp);
+  e = cudaGetLastError();
+  log.mark();
+  if (e != cudaSuccess) return e;
+  return launch_acc_to_bf16(ws.acc, dq, p.elems(), log);
+}
+
+}  // namespace
+
+cudaError_t tc_forward(const Problem& p, const void* q, const void* k, const void* v, void* o,
+                       float* lse, const Workspace& ws, LaunchLog& log) {
+  if (p.d == 128) return forward_d<128>(p, q, k, v, o, lse, ws, log);
+  return forward_d<64>(p, q, k, v, o, lse, ws, log);
+}
+
+cudaError_t tc_backward(const Problem& p, const void* q, const void* k, const void* v,
+                        const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                        void* dv, const Workspace& ws, LaunchLog& log) {
+  if (p.d == 128) return backward_d<128>(p, q, k, v, o, lse, dO, dq, dk, dv, ws, log);
+  return backward_d<64>(p, q, k, v, o, lse, dO, dq, dk, dv, ws, log);
+}
+
+}  // namespace fbob

@@ -1,0 +1,144 @@
+// Shared pieces of the tensor-core kernels (BoB passes, forward, first
+// backward): bounded waits, tile visiting order, TMA tile loads, descriptor
+// offset arithmetic, and the host-side tensor-map encoder.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm103.cuh"
+
+namespace fbob {
+namespace tc {
+
+using namespace sm103;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// MN-major operand descriptor convention: LBO = stride between 64-element
+// groups along M/N, SBO = stride between 8-row groups along K.
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        report_status(status, FBOB_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform bounded wait: tcgen05.ld is .sync.aligned, so every lane of
+// a warp must take the same branch after a wait.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  const bool ok = wait_bar(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Named barrier over the first THREADS threads of the CTA (id != 0).
+template <int THREADS>
+__device__ __forceinline__ void named_sync(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(THREADS) : "memory");
+}
+
+// Tile visited at step t when a CTA starts its loop at tile `rot` and wraps:
+// CTAs of one head sweep the shared operand tiles out of phase, so the L2
+// serves a tile to a few SMs at a time instead of to all of them at once.
+// Every sum over tiles is order-independent.
+__device__ __forceinline__ int rotated(int t, int rot, int T) {
+  const int u = t + rot;
+  return u >= T ? u - T : u;
+}
+
+// One TMA box per [rows][D] tile: the 4-D tensor view (64 features, rows,
+// D/64 feature halves, heads) lands it as D/64 consecutive [rows][64] blocks.
+__device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, uint64_t* bar, int row,
+                                          int bh) {
+  tma_load_4d(dst, map, bar, 0, row, 0, bh);
+}
+
+// Two [rows][D] tiles A and B interleaved per 64-feature half (A_h, B_h,
+// A_h+1, ...): each half holds 2*rows rows, so one N = 2*rows MMA sees A and B
+// stacked.  Maps with one feature half per box.
+template <int D>
+__device__ __forceinline__ void load_pair(uint8_t* dst, const CUtensorMap* mapA,
+                                          const CUtensorMap* mapB, uint64_t* bar, int rows, int row,
+                                          int bh) {
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) {
+    tma_load_4d(dst + h * 2 * rows * 128, mapA, bar, 0, row, h, bh);
+    tma_load_4d(dst + h * 2 * rows * 128 + rows * 128, mapB, bar, 0, row, h, bh);
+  }
+}
+
+// K-major tile [rows][D] stored as D/64 boxes of [rows][64] (128 B rows,
+// 128-byte swizzle): offset of the k-th 16-element slice along D, in
+// descriptor units (16 bytes), to add to the tile's descriptor low word.
+__host__ __device__ constexpr uint32_t kslice_off(int rows, int k) {
+  return (uint32_t)(((k >> 2) * rows * 128 + (k & 3) * 32) >> 4);
+}
+// MN-major operand: the k-th 16-row step along K (16 rows x 128 B).
+__host__ __device__ constexpr uint32_t kstep_off(int k) { return (uint32_t)(k * 2048 >> 4); }
+// A value the compiler must treat as new on every evaluation: keeps
+// `base + constant` descriptor words inside the tile loop (one add each)
+// instead of hoisting every unrolled offset into its own register.
+__device__ __forceinline__ uint32_t opaque(uint32_t x) {
+  asm volatile("" : "+r"(x));
+  return x;
+}
+// Descriptor low words (see sdesc_lo).
+__device__ __forceinline__ uint32_t lo_kmajor(uint32_t saddr) { return sdesc_lo(saddr, 16); }
+__device__ __forceinline__ uint32_t lo_mnmajor(uint32_t saddr, uint32_t mn_group_stride) {
+  return sdesc_lo(saddr, mn_group_stride);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [B*H, N, D] bf16 tensor viewed 4-D as (64 features, N rows, D/64 halves,
+// B*H heads); one box = box_rows rows x all D features, landing in shared
+// memory as D/64 consecutive [box_rows][64] blocks with 128-byte swizzle.
+// Rows past N read as zero.
+// With one_half the box spans a single 64-feature half (for interleaved pairs).
+inline bool make_map(CUtensorMap* m, const void* ptr, const Problem& p, int box_rows,
+                     bool one_half = false) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {64, (cuuint64_t)p.N, (cuuint64_t)(p.d / 64), (cuuint64_t)p.BH()};
+  cuuint64_t strides[3] = {(cuuint64_t)p.d * 2, 128, (cuuint64_t)p.N * p.d * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, one_half ? 1u : (cuuint32_t)(p.d / 64), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+}  // namespace fbob

@@ -99,18 +99,36 @@ def test_null_and_misaligned_pointers_rejected(lib):
 
 
 def test_kernel_family_choice(lib):
-    fp32 = shape(dtype=1)
-    assert lib.fbob_path(2, ctypes.byref(fp32)) == fbob.PATH_SIMT
-    odd = shape(d=40)
-    assert lib.fbob_path(2, ctypes.byref(odd)) == fbob.PATH_SIMT
-    for d in (64, 128):
-        s = shape(d=d)
-        assert lib.fbob_path(2, ctypes.byref(s)) in (fbob.PATH_SIMT, fbob.PATH_TCGEN05)
+    """bf16 at d = 64 / 128 takes the tcgen05 kernels for all three calls;
+    fp32 and other head sizes take the CUDA-core kernels."""
+    for op in (fbob.OP_FORWARD, fbob.OP_BACKWARD, fbob.OP_BOB):
+        fp32 = shape(dtype=1)
+        assert lib.fbob_path(op, ctypes.byref(fp32)) == fbob.PATH_SIMT
+        odd = shape(d=40)
+        assert lib.fbob_path(op, ctypes.byref(odd)) == fbob.PATH_SIMT
+        for d in (64, 128):
+            assert lib.fbob_path(op, ctypes.byref(shape(d=d))) == fbob.PATH_TCGEN05
     old = lib.fbob_force_path(0)
     try:
-        assert lib.fbob_path(2, ctypes.byref(shape(d=128))) == fbob.PATH_SIMT
+        for op in (fbob.OP_FORWARD, fbob.OP_BACKWARD, fbob.OP_BOB):
+            assert lib.fbob_path(op, ctypes.byref(shape(d=128))) == fbob.PATH_SIMT
     finally:
         lib.fbob_force_path(old)
+
+
+def test_workspace_sizes_per_family(lib):
+    """The tcgen05 first backward and BoB need the fp32 dQ / gradQ accumulator
+    (B*H*N*d*4 bytes) on top of the row scalars; the forward needs only the
+    status word."""
+    s = shape(d=128)
+    rows = s.B * s.H * s.N
+    acc = rows * s.d * 4
+    fwd = lib.fbob_workspace_size(fbob.OP_FORWARD, ctypes.byref(s))
+    bwd = lib.fbob_workspace_size(fbob.OP_BACKWARD, ctypes.byref(s))
+    bob = lib.fbob_workspace_size(fbob.OP_BOB, ctypes.byref(s))
+    assert fwd == 256
+    assert bwd >= 256 + rows * 4 + acc
+    assert bob >= 256 + 3 * rows * 4 + acc
 
 
 def test_profile_event_hook_validation(lib):
