@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     workspace_size,
 )
 from .autograd import attention  # noqa: F401
+from . import meta  # noqa: F401
 from .build import build_library  # noqa: F401
 
 __version__ = "0.1.0"
