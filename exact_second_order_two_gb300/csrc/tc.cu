@@ -75,13 +75,18 @@ struct Row {
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "pass 1 shared memory budget");
-  // TMEM columns: S and G (one buffer; the elementwise warps free it right
-  // after loading), W, bf16 P and P*G (two buffers), and the stationary bf16
-  // Q and gQ as MMA A operands (D/2 columns each)
-  static constexpr uint32_t T_S = 0, T_G = 64, T_W = 128, TMEM_COLS = 512;
-  __host__ __device__ static constexpr uint32_t T_P(int b) { return 256u + 64u * b; }
-  __host__ __device__ static constexpr uint32_t T_PG(int b) { return 256u + 64u * b + 32u; }
-  static constexpr uint32_t T_QA = 384, T_GQA = 384 + D / 2;
+  // TMEM columns: two [S | G] buffers (64 + 64 columns), W, and the
+  // stationary bf16 Q and gQ as MMA A operands (D/2 columns each).  The
+  // elementwise warps write bf16 P and P*G back into the first 16 of the 32 S
+  // and G columns each of them read: the A operands of the W MMAs.  While
+  // they work on one buffer, the S/G MMAs of the next tile fill the other.
+  static constexpr uint32_t T_W = 256, TMEM_COLS = 512;
+  __host__ __device__ static constexpr uint32_t T_S(int b) { return 128u * b; }
+  __host__ __device__ static constexpr uint32_t T_G(int b) { return 128u * b + 64u; }
+  // bf16 P (or P*G) of keys [16k, 16k + 16): column offset in the S (G) block
+  __host__ __device__ static constexpr uint32_t p_col(int k) { return 32u * (k >> 1) + 8u * (k & 1); }
+  static constexpr uint32_t T_QA = 256 + D, T_GQA = 256 + D + D / 2;
+  static_assert(T_GQA + D / 2 <= TMEM_COLS, "pass 1 TMEM budget");
 };
 
 struct RowParams {
@@ -117,11 +122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kg_empty = kg_full + C::STAGES;      // [STAGES]
   uint64_t* v_full = kg_empty + C::STAGES;       // [VSTAGES]
   uint64_t* v_empty = v_full + C::VSTAGES;       // [VSTAGES]
-  uint64_t* sg_full = v_empty + C::VSTAGES;      // [2]
-  uint64_t* sg_empty = sg_full + 2;              // [2]
-  uint64_t* p_full = sg_empty + 2;               // [2]
-  uint64_t* p_empty = p_full + 2;                // [2]
-  uint64_t* w_done = p_empty + 2;
+  uint64_t* sg_full = v_empty + C::VSTAGES;      // [2]: S, G of a buffer in TMEM
+  uint64_t* p_full = sg_full + 2;                // [2]: bf16 P, P*G of a buffer in TMEM
+  uint64_t* w_done = p_full + 2;
   uint64_t* q_tmem = w_done + 2;                  // Q, gQ copied into TMEM
   uint64_t* drain = w_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
@@ -151,9 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sg_full + b, 1);
-      mbar_init(sg_empty + b, kConsumers);
       mbar_init(p_full + b, kConsumers);
-      mbar_init(p_empty + b, 1);
     }
     mbar_init(w_done, 1);
     mbar_init(drain, 1);
@@ -227,34 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // Q [K;gK]^T: N=128
       constexpr uint32_t id_w = idesc_bf16(128, D, false, true);    // W: N=D, B MN-major
       bool ok = wait_bar(q_tmem, 0, abort_flag, prm.status);
-      // W += P gV + (P*G) V for tile t: A operands (bf16 P, P*G) from TMEM
-      auto issue_w = [&](int t) -> bool {
-        const int s = t % C::VSTAGES, b = t & 1;
-        if (!wait_bar(p_full + b, (t >> 1) & 1, abort_flag, prm.status)) return false;
-        if (!wait_bar(v_full + s, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
-        tc_fence_after();
-        const uint32_t st = sb + C::OFF_V + s * C::SB;
-        const uint32_t v_lo = lo_mnmajor(st, C::BN * 128), gv_lo = lo_mnmajor(st + C::KB, C::BN * 128);
-        const uint32_t tw = tmem + C::T_W, tp = tmem + C::T_P(b), tpg = tmem + C::T_PG(b);
-        const uint32_t first = t > 0 ? 1u : 0u;
-#pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 keys
-          mma_ts(tw, tp + 8 * k, gv_lo + kstep_off(k), id_w, k > 0 ? 1u : first);
-          mma_ts(tw, tpg + 8 * k, v_lo + kstep_off(k), id_w, 1u);
-        }
-        mma_commit(p_empty + b);
-        mma_commit(v_empty + s);
-        return true;
-      };
-      for (int t = 0; ok && t < T; ++t) {
-        const int s = t % C::STAGES;
-        if (!wait_bar(kg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
-        if (t >= 1 && !wait_bar(sg_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+      const uint32_t tw = tmem + C::T_W, tq = tmem + C::T_QA, tgq = tmem + C::T_GQA;
+      // S and G of tile t into buffer t & 1
+      auto issue_sg = [&](int t) -> bool {
+        const int s = t % C::STAGES, b = t & 1;
+        if (!wait_bar(kg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
         // [K;gK] per half, 2*BN rows
-        const uint32_t kgk_lo = lo_kmajor(sb + C::OFF_KG + s * C::SB);
-        const uint32_t ts = tmem + C::T_S, tg = tmem + C::T_G, tq = tmem + C::T_QA,
-                       tgq = tmem + C::T_GQA;
+        const uint32_t kgk_lo = opaque(lo_kmajor(sb + C::OFF_KG + s * C::SB));
+        const uint32_t ts = tmem + C::T_S(b), tg = tmem + C::T_G(b);
         // [S | Q gK^T] = Q [K; gK]^T in one N=128 MMA chain (T_G = T_S + 64),
         // A = Q from TMEM
 #pragma unroll
@@ -264,11 +246,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_ts(tg, tgq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_s, 1u);
-        mma_commit(sg_full);
+        mma_commit(sg_full + b);
         mma_commit(kg_empty + s);
-        if (t >= 1 && !issue_w(t - 1)) { ok = false; break; }
+        return true;
+      };
+      // W += P gV + (P*G) V for tile t: A operands (bf16 P, P*G) from TMEM
+      auto issue_w = [&](int t) -> bool {
+        const int s = t % C::VSTAGES, b = t & 1;
+        if (!wait_bar(p_full + b, (t >> 1) & 1, abort_flag, prm.status)) return false;
+        if (!wait_bar(v_full + s, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
+        tc_fence_after();
+        const uint32_t st = sb + C::OFF_V + s * C::SB;
+        const uint32_t v_lo = opaque(lo_mnmajor(st, C::BN * 128)),
+                       gv_lo = opaque(lo_mnmajor(st + C::KB, C::BN * 128));
+        const uint32_t tp = tmem + C::T_S(b), tpg = tmem + C::T_G(b);
+        const uint32_t first = t > 0 ? 1u : 0u;
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 keys
+          mma_ts(tw, tp + C::p_col(k), gv_lo + kstep_off(k), id_w, k > 0 ? 1u : first);
+          mma_ts(tw, tpg + C::p_col(k), v_lo + kstep_off(k), id_w, 1u);
+        }
+        mma_commit(v_empty + s);
+        return true;
+      };
+      // Buffer b holds tile t until the W MMAs of t have read its P: the S/G
+      // MMAs of tile t + 2 are issued after them, and MMAs from one thread
+      // run in issue order.
+      ok = ok && issue_sg(0) && (T < 2 || issue_sg(1));
+      for (int t = 0; ok && t < T; ++t) {
+        if (!issue_w(t)) { ok = false; break; }
+        if (t + 2 < T && !issue_sg(t + 2)) { ok = false; break; }
       }
-      if (ok && issue_w(T - 1)) mma_commit(w_done);
+      if (ok) mma_commit(w_done);
       // every MMA this thread issued has completed before TMEM is released
       mma_commit(drain);
       mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
@@ -312,13 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; ok && t < T; ++t) {
       const int b = t & 1;
-      if (!warp_wait(sg_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+      // buffer b last held tile t - 2, whose W MMAs completed before the S/G
+      // MMAs of tile t (issued after them) signalled sg_full
+      if (!warp_wait(sg_full + b, (t >> 1) & 1, abort_flag, prm.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[32], gr[32];
-      tmem_ld32x2(tmem + lane_off + C::T_S + 32 * half, tmem + lane_off + C::T_G + 32 * half, sr,
-                  gr);
-      tc_fence_before();
-      mbar_arrive(sg_empty);
+      const uint32_t ts = tmem + lane_off + C::T_S(b) + 32 * half,
+                     tg = tmem + lane_off + C::T_G(b) + 32 * half;
+      tmem_ld32x2(ts, tg, sr, gr);
       const int j0 = rotated(t, rot, T) * C::BN + 32 * half;
       const bool need_mask = !row_ok || (j0 + 32 > N) || (prm.causal && j0 + 31 > i0);
       uint32_t pw[16], pgw[16];
@@ -343,16 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         body(std::true_type{});
       else
         body(std::false_type{});
-      keep16(pw);  // finish the elementwise work before waiting for the P buffer
-      keep16(pgw);
-      // P buffer b was last read by the W MMAs of tile t-2
-      if (t >= 2 && !warp_wait(p_empty + b, ((t >> 1) - 1) & 1, abort_flag, prm.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st16(tmem + lane_off + C::T_P(b) + 16 * half, pw);
-      tmem_st16(tmem + lane_off + C::T_PG(b) + 16 * half, pgw);
+      // bf16 P and P*G of this thread's 32 keys into the first 16 of the S and
+      // G columns it just read (keys 32*half + 2c, + 1 in column c)
+      tmem_st16(ts, pw);
+      tmem_st16(tg, pgw);
       tc_fence_before();
       mbar_arrive(p_full + b);
     }
