@@ -116,6 +116,8 @@ def _check_tensors(ref: torch.Tensor, named: dict, scalar_names=()):
     if not ref.is_cuda:
         raise ValueError("tensors must be CUDA tensors")
     for name, t in named.items():
+        if t is None:  # an optional argument left out
+            continue
         if t.device != ref.device:
             raise ValueError(f"{name} is on {t.device}, expected {ref.device}")
         if not t.is_contiguous():
@@ -197,7 +199,8 @@ def backward(q, k, v, o, lse, do, causal: bool = False,
 def bob(q, k, v, o, lse, do, gq, gk, gv, causal: bool = False,
         scale: float | None = None, out=None, workspace=None):
     """Backward-over-backward: returns (gradQ, gradK, gradV, graddO), the
-    gradient of <gQ,dQ> + <gK,dK> + <gV,dV> w.r.t. (Q, K, V, dO)."""
+    gradient of <gQ,dQ> + <gK,dK> + <gV,dV> w.r.t. (Q, K, V, dO).  Any of gq,
+    gk, gv may be None: a zero cotangent, whose work the kernels skip."""
     _check_tensors(q, {"k": k, "v": v, "o": o, "do": do, "gq": gq, "gk": gk,
                        "gv": gv, "lse": lse}, ("lse",))
     shp = shape_of(q, causal, scale)

@@ -37,13 +37,17 @@ class _AttentionBackward(torch.autograd.Function):
         dq, dk, dv = _b.backward(q, k, v, o, lse, do, causal, scale)
         ctx.save_for_backward(q, k, v, do, o, lse)
         ctx.causal, ctx.scale = causal, scale
+        # a second-order loss that reads only some of dQ, dK, dV leaves the
+        # other cotangents None; fbob_bob skips their work
+        ctx.set_materialize_grads(False)
         return dq, dk, dv
 
     @staticmethod
     def backward(ctx, gq, gk, gv):
         q, k, v, do, o, lse = ctx.saved_tensors
-        # autograd materialises unused cotangents as zeros
-        gq, gk, gv = (_contig(g) for g in (gq, gk, gv))
+        if gq is None and gk is None and gv is None:
+            return None, None, None, None, None, None, None, None
+        gq, gk, gv = (None if g is None else _contig(g) for g in (gq, gk, gv))
         gradq, gradk, gradv, graddo = _b.bob(q, k, v, o, lse, do, gq, gk, gv,
                                              ctx.causal, ctx.scale)
         return gradq, gradk, gradv, graddo, None, None, None, None

@@ -99,6 +99,12 @@ bool ptrs_ok(std::initializer_list<const void*> ps) {
   return true;
 }
 
+bool opt_ptrs_ok(std::initializer_list<const void*> ps) {
+  for (const void* q : ps)
+    if (q && !aligned16(q)) return false;
+  return true;
+}
+
 }  // namespace
 
 void LaunchLog::mark() {
@@ -205,12 +211,21 @@ int fbob_bob(const fbob_shape_t* shape, const void* q, const void* k,
   int path;
   Workspace ws;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (!ptrs_ok({q, k, v, o, lse, dO, gq, gk, gv, gradq, gradk, gradv, graddo}))
+  // gq, gk, gv may be null (a zero cotangent); present ones must be aligned
+  if (!ptrs_ok({q, k, v, o, lse, dO, gradq, gradk, gradv, graddo}) || !opt_ptrs_ok({gq, gk, gv}))
     return FBOB_ERR_INVALID_ARG;
   int st = prologue(FBOB_OP_BOB, shape, ws_ptr, ws_bytes, s, &p, &path, &ws);
   if (st != FBOB_OK) return st;
   LaunchLog log{s};
   if (g_event_count > 0) cudaEventRecord(g_events[0], s);
+  if (!gq && !gk && !gv) {  // L = 0: every output is zero
+    const size_t bytes = p.elems() * (p.bf16 ? 2 : 4);
+    cudaError_t e = cudaSuccess;
+    for (void* out : {gradq, gradk, gradv, graddo})
+      if (e == cudaSuccess) e = cudaMemsetAsync(out, 0, bytes, s);
+    g_last_launches = 0;
+    return to_status(e);
+  }
   cudaError_t e =
       path == FBOB_PATH_TCGEN05
           ? tc_bob(p, q, k, v, o, lse, dO, gq, gk, gv, gradq, gradk, gradv, graddo, ws, log)

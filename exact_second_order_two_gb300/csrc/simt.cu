@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     const bool ok = ii < N;
     const size_t off = base + (size_t)(ok ? ii : 0) * d + c;
     qs[e] = ok ? ldx<T>(a.q, off) : 0.f;
-    if (kNeedGq) gqs[e] = ok ? ldx<T>(a.gq, off) : 0.f;
+    if (kNeedGq) gqs[e] = ok && a.gq ? ldx<T>(a.gq, off) : 0.f;  // null: zero cotangent
     if (kNeedDo) dos[e] = ok ? ldx<T>(a.dO, off) : 0.f;
   }
   float lse_i = 0.f, D_i = 0.f, r_i = 0.f, sig_i = 0.f;
@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(kWarps * 32)
       ks[jj * ldk + c] = ok ? ldx<T>(a.k, off) : 0.f;
       vs[jj * ldk + c] = ok ? ldx<T>(a.v, off) : 0.f;
       if (kNeedGkv) {
-        gks[jj * ldk + c] = ok ? ldx<T>(a.gk, off) : 0.f;
-        gvs[jj * ldk + c] = ok ? ldx<T>(a.gv, off) : 0.f;
+        gks[jj * ldk + c] = ok && a.gk ? ldx<T>(a.gk, off) : 0.f;
+        gvs[jj * ldk + c] = ok && a.gv ? ldx<T>(a.gv, off) : 0.f;
       }
     }
     __syncthreads();
@@ -302,8 +302,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     ks[e] = ok ? ldx<T>(a.k, off) : 0.f;
     vs[e] = ok ? ldx<T>(a.v, off) : 0.f;
     if (kBob) {
-      gks[e] = ok ? ldx<T>(a.gk, off) : 0.f;
-      gvs[e] = ok ? ldx<T>(a.gv, off) : 0.f;
+      gks[e] = ok && a.gk ? ldx<T>(a.gk, off) : 0.f;
+      gvs[e] = ok && a.gv ? ldx<T>(a.gv, off) : 0.f;
     }
   }
 
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       const size_t off = base + (size_t)(ok ? i : 0) * d + c;
       qs[ii * ldk + c] = ok ? ldx<T>(a.q, off) : 0.f;
       dos[ii * ldk + c] = ok ? ldx<T>(a.dO, off) : 0.f;
-      if (kBob) gqs[ii * ldk + c] = ok ? ldx<T>(a.gq, off) : 0.f;
+      if (kBob) gqs[ii * ldk + c] = ok && a.gq ? ldx<T>(a.gq, off) : 0.f;
     }
     if (threadIdx.x < kTile) {
       const int i = i0 + threadIdx.x;

@@ -53,6 +53,19 @@ constexpr int kThreads = 320;
 constexpr int kConsumers = kConsumerWarps * 32;
 __device__ __forceinline__ void consumer_sync() { named_sync<kConsumers>(1); }
 
+// [K|gK] (or [Q|gQ]) pair stage: the second tensor is skipped when its
+// cotangent is absent (the MMAs then read only the first BN rows per half).
+template <int D>
+__device__ __forceinline__ void load_pair_opt(uint8_t* dst, const CUtensorMap* mapA,
+                                              const CUtensorMap* mapB, bool with_b, uint64_t* bar,
+                                              int rows, int row, int bh) {
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) {
+    tma_load_4d(dst + h * 2 * rows * 128, mapA, bar, 0, row, h, bh);
+    if (with_b) tma_load_4d(dst + h * 2 * rows * 128 + rows * 128, mapB, bar, 0, row, h, bh);
+  }
+}
+
 // ===========================================================================
 // Pass 1: row-stationary.
 // ===========================================================================
@@ -101,15 +114,22 @@ struct RowParams {
   int* status;
   int N, causal;
   float scale;
+  // which cotangents are present (an absent one is zero: its loads and MMAs
+  // are skipped); at least one is
+  int has_gq, has_gk, has_gv;
 };
 
-template <int D>
+template <int D, bool ALL>
 __global__ void __launch_bounds__(kThreads, 1)
     bob_row_pass(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mGQ,
                  const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mGK,
                  const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mGV,
                  RowParams prm) {
   using C = Row<D>;
+  // cotangents present: ALL (every one) is the compiled fast path; otherwise
+  // the flags decide at run time
+  const bool has_gq = ALL || prm.has_gq != 0, has_gk = ALL || prm.has_gk != 0,
+             has_gv = ALL || prm.has_gv != 0;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
   if (sb & 1023u) {  // 128-byte swizzled tiles need a 1024-byte aligned base
@@ -175,9 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mK);
-      mbar_arrive_expect_tx(q_full, 2 * C::QB);
+      mbar_arrive_expect_tx(q_full, (has_gq ? 2 : 1) * C::QB);
       load_tile(smem + C::OFF_Q, &mQ, q_full, i0, bh);
-      load_tile(smem + C::OFF_GQ, &mGQ, q_full, i0, bh);
+      if (has_gq) load_tile(smem + C::OFF_GQ, &mGQ, q_full, i0, bh);
       // [K|gK] runs one tile ahead of [V|gV]: the S/G MMAs of tile t+1 need
       // only K/gK, which are released as soon as the S/G MMAs of tile t-1 end
       int kg_issued = 0, v_issued = 0;
@@ -187,9 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             !wait_bar(kg_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status))
           return false;
         uint8_t* st = smem + C::OFF_KG + s * C::SB;
-        mbar_arrive_expect_tx(kg_full + s, C::SB);
+        mbar_arrive_expect_tx(kg_full + s, has_gk ? C::SB : C::SB / 2);
         const int kt = rotated(t, rot, T) * C::BN;
-        load_pair<D>(st, &mK, &mGK, kg_full + s, C::BN, kt, bh);
+        load_pair_opt<D>(st, &mK, &mGK, has_gk, kg_full + s, C::BN, kt, bh);
         ++kg_issued;
         return true;
       };
@@ -199,10 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             !wait_bar(v_empty + s, ((t / C::VSTAGES) - 1) & 1, abort_flag, prm.status))
           return false;
         uint8_t* st = smem + C::OFF_V + s * C::SB;
-        mbar_arrive_expect_tx(v_full + s, C::SB);
+        mbar_arrive_expect_tx(v_full + s, has_gv ? C::SB : C::KB);
         const int kt = rotated(t, rot, T) * C::BN;
         load_tile(st, &mV, v_full + s, kt, bh);
-        load_tile(st + C::KB, &mGV, v_full + s, kt, bh);
+        if (has_gv) load_tile(st + C::KB, &mGV, v_full + s, kt, bh);
         ++v_issued;
         return true;
       };
@@ -238,14 +258,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kgk_lo = opaque(lo_kmajor(sb + C::OFF_KG + s * C::SB));
         const uint32_t ts = tmem + C::T_S(b), tg = tmem + C::T_G(b);
         // [S | Q gK^T] = Q [K; gK]^T in one N=128 MMA chain (T_G = T_S + 64),
-        // A = Q from TMEM
+        // A = Q from TMEM; S = Q K^T alone (N=64) without gK
+        const uint32_t id_first = has_gk ? id_sg : id_s;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ts(ts, tq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_sg, k > 0 ? 1u : 0u);
+          mma_ts(ts, tq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_first, k > 0 ? 1u : 0u);
         // G += gQ K^T (the first BN rows of each [K;gK] half are K), A = gQ from TMEM
+        if (has_gq) {
+          const uint32_t g0 = has_gk ? 1u : 0u;  // without gK this starts G
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ts(tg, tgq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_s, 1u);
+          for (int k = 0; k < D / 16; ++k)
+            mma_ts(tg, tgq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_s, k > 0 ? 1u : g0);
+        }
         mma_commit(sg_full + b);
         mma_commit(kg_empty + s);
         return true;
@@ -261,10 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                        gv_lo = opaque(lo_mnmajor(st + C::KB, C::BN * 128));
         const uint32_t tp = tmem + C::T_S(b), tpg = tmem + C::T_G(b);
         const uint32_t first = t > 0 ? 1u : 0u;
+        // without gV only (P*G) V; without gQ and gK, G = 0 and only P gV
+        const bool use_gv = has_gv, use_g = has_gq || has_gk;
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 keys
-          mma_ts(tw, tp + C::p_col(k), gv_lo + kstep_off(k), id_w, k > 0 ? 1u : first);
-          mma_ts(tw, tpg + C::p_col(k), v_lo + kstep_off(k), id_w, 1u);
+          const uint32_t acc = k > 0 ? 1u : first;
+          if (use_gv) mma_ts(tw, tp + C::p_col(k), gv_lo + kstep_off(k), id_w, acc);
+          if (use_g) mma_ts(tw, tpg + C::p_col(k), v_lo + kstep_off(k), id_w, use_gv ? 1u : acc);
         }
         mma_commit(v_empty + s);
         return true;
@@ -292,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lse2 = row_ok ? prm.lse[srow] * kLog2e : 0.f;
     const float sc2 = prm.scale * kLog2e;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const bool has_g = has_gq || has_gk;
     float r_acc = 0.f;
     bool ok = warp_wait(q_full, 0, abort_flag, prm.status);
     if (ok) {
@@ -301,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int which = 0; which < 2; ++which) {
         const int h = D == 128 ? half : 0;          // feature half copied
         if (D == 64 && which != half) continue;     // d = 64: half 0 -> Q, half 1 -> gQ
+        if (which == 1 && !has_gq) continue;    // no gQ: its TMEM copy is never read
         const uint32_t src = sb + (which == 0 ? C::OFF_Q : C::OFF_GQ) + h * C::BM * 128 + row * 128;
         uint32_t w[32];
 #pragma unroll
@@ -342,8 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             p0 = (row_ok && jj < N && (!prm.causal || jj <= i)) ? p0 : 0.f;
             p1 = (row_ok && jj + 1 < N && (!prm.causal || jj + 1 <= i)) ? p1 : 0.f;
           }
-          const float g0 = p0 * (__uint_as_float(gr[c]) * prm.scale);
-          const float g1 = p1 * (__uint_as_float(gr[c + 1]) * prm.scale);
+          // G is zero (and its TMEM columns unwritten) without gQ and gK
+          const float g0 = has_g ? p0 * (__uint_as_float(gr[c]) * prm.scale) : 0.f;
+          const float g1 = has_g ? p1 * (__uint_as_float(gr[c + 1]) * prm.scale) : 0.f;
           r_acc += g0 + g1;
           pw[c >> 1] = pack_bf16(p0, p1);
           pgw[c >> 1] = pack_bf16(g0, g1);
@@ -469,6 +499,7 @@ struct ColParams {
   int* status;
   int N, causal;
   float scale;
+  int has_gq, has_gk, has_gv;  // as in RowParams
 };
 
 // Pass 2 warp roles: warps 0-15 elementwise (warp w: TMEM lane quadrant w%4,
@@ -483,13 +514,17 @@ constexpr int kColThreads = (kColConsumerWarps + 2) * 32;
 constexpr int kColCols = 64 / (kColConsumerWarps / 4);  // columns per elementwise thread
 static_assert(kColCols == 16, "one 16-query MMA step per column slice");
 
-template <int D>
+template <int D, bool ALL>
 __global__ void __launch_bounds__(kColThreads, 1)
     bob_col_pass(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mGK,
                  const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mGV,
                  const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mGQ,
                  const __grid_constant__ CUtensorMap mDO, ColParams prm) {
   using C = Col<D>;
+  // cotangents present: ALL (every one) is the compiled fast path; otherwise
+  // the flags decide at run time
+  const bool has_gq = ALL || prm.has_gq != 0, has_gk = ALL || prm.has_gk != 0,
+             has_gv = ALL || prm.has_gv != 0;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
   if (sb & 1023u) {  // 128-byte swizzled tiles need a 1024-byte aligned base
@@ -550,11 +585,11 @@ __global__ void __launch_bounds__(kColThreads, 1)
 
   if (warp == kColProducerWarp) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(kv_full, 4 * C::KB);
+      mbar_arrive_expect_tx(kv_full, (2 + (has_gk ? 1 : 0) + (has_gv ? 1 : 0)) * C::KB);
       load_tile(smem + C::OFF_K, &mK, kv_full, j0, bh);
-      load_tile(smem + C::OFF_GK, &mGK, kv_full, j0, bh);
+      if (has_gk) load_tile(smem + C::OFF_GK, &mGK, kv_full, j0, bh);
       load_tile(smem + C::OFF_V, &mV, kv_full, j0, bh);
-      load_tile(smem + C::OFF_GV, &mGV, kv_full, j0, bh);
+      if (has_gv) load_tile(smem + C::OFF_GV, &mGV, kv_full, j0, bh);
     }
     bool ok = true;
     // row scalars (lse pre-scaled by log2 e, D, r, sigma) of the next query
@@ -603,12 +638,13 @@ __global__ void __launch_bounds__(kColThreads, 1)
         for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = pre[a][u];
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(qg_full + s, 2 * C::QB);
-        load_pair<D>(smem + C::OFF_QG + s * 2 * C::QB, &mQ, &mGQ, qg_full + s, C::BN, q0, bh);
+        mbar_arrive_expect_tx(qg_full + s, (has_gq ? 2 : 1) * C::QB);
+        load_pair_opt<D>(smem + C::OFF_QG + s * 2 * C::QB, &mQ, &mGQ, has_gq, qg_full + s,
+                         C::BN, q0, bh);
         ++qg_issued;
         if (t + 1 < T) {  // warm L2 with the next query tile
           tma_prefetch_l2_4d(&mQ, 0, q_next, 0, bh);
-          tma_prefetch_l2_4d(&mGQ, 0, q_next, 0, bh);
+          if (has_gq) tma_prefetch_l2_4d(&mGQ, 0, q_next, 0, bh);
           tma_prefetch_l2_4d(&mDO, 0, q_next, 0, bh);
         }
       }
@@ -653,21 +689,30 @@ __global__ void __launch_bounds__(kColThreads, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_ss(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc, k > 0 ? 1u : 0u);
+        if (has_gv) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ss(t_h, gv_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc, k > 0 ? 1u : 0u);
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(t_h, gv_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
+                   k > 0 ? 1u : 0u);
+        }
         if (!wait_bar(qg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
         if (C::GQ_IN_S && t >= 1 && !wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status))
           return false;
         tc_fence_after();
-        // [S^T | K gQ^T] = K [Q; gQ]^T, then G^T += gK Q^T (first BN rows per half)
+        // [S^T | K gQ^T] = K [Q; gQ]^T (S^T = K Q^T alone without gQ), then
+        // G^T += gK Q^T (the first BN rows of each [Q;gQ] half are Q)
+        const uint32_t id_first = has_gq ? id_sg : id_sc;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(t_s, k_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_sg,
+          mma_ss(t_s, k_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_first,
                  k > 0 ? 1u : 0u);
+        if (has_gk) {
+          const uint32_t g0 = has_gq ? 1u : 0u;  // without gQ this starts G^T
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ss(t_g, gk_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_sc, 1u);
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(t_g, gk_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_sc,
+                   k > 0 ? 1u : g0);
+        }
         mma_commit(sc_full);
         return true;
       };
@@ -690,7 +735,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 queries
           mma_ts(t_gk, t_g + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-          mma_ts(t_gk, t_dp + 16 * k, gq_mn + kstep_off(k), id_out, 1u);
+          if (has_gq) mma_ts(t_gk, t_dp + 16 * k, gq_mn + kstep_off(k), id_out, 1u);
         }
         mma_commit(qg_empty + s);
 #pragma unroll
@@ -704,7 +749,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
 #pragma unroll
         for (int k = 0; k < C::BM / 16; ++k) {  // contraction over the 128 keys
           mma_ss(t_gq, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
-          mma_ss(t_gq, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
+          if (has_gk) mma_ss(t_gq, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
         }
         mma_commit(gq_full);
         // the next tile's scores overwrite the A operands read above; MMAs
@@ -723,6 +768,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
     const int j = j0 + row;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sc2 = prm.scale * kLog2e;
+    const bool has_g = has_gq || has_gk, has_h = has_gv;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
@@ -757,10 +803,12 @@ __global__ void __launch_bounds__(kColThreads, 1)
               p = (q < N && j < N && (!prm.causal || q >= j)) ? p : 0.f;
             }
             const float dpm = __uint_as_float(dpr[cc]) - dv[e];
-            const float gm = fmaf(__uint_as_float(gr[cc]), prm.scale, -rv[e]);
+            // G^T (H^T) is zero, its TMEM columns unwritten, without gQ and gK (gV)
+            const float gm = has_g ? fmaf(__uint_as_float(gr[cc]), prm.scale, -rv[e]) : -rv[e];
+            const float hv = has_h ? __uint_as_float(hr[cc]) : 0.f;
             o_ds[e] = p * dpm;
             o_gd[e] = p * gm;
-            o_gs[e] = p * (fmaf(gm, dpm, __uint_as_float(hr[cc])) - sv[e]);
+            o_gs[e] = p * (fmaf(gm, dpm, hv) - sv[e]);
           }
           dsw[2 * c4] = pack_bf16(o_ds[0], o_ds[1]);
           dsw[2 * c4 + 1] = pack_bf16(o_ds[2], o_ds[3]);
@@ -877,22 +925,28 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
                   const Workspace& ws, LaunchLog& log) {
   using R = Row<D>;
   using Cc = Col<D>;
+  // an absent cotangent (null pointer) is zero: its map is a placeholder the
+  // kernels never load through
+  const int has_gq = gq != nullptr, has_gk = gk != nullptr, has_gv = gv != nullptr;
   CUtensorMap mQr, mGQr, mKr, mGKr, mVr, mGVr;
-  if (!make_map(&mQr, q, p, R::BM) || !make_map(&mGQr, gq, p, R::BM) ||
-      !make_map(&mKr, k, p, R::BN, true) || !make_map(&mGKr, gk, p, R::BN, true) ||
-      !make_map(&mVr, v, p, R::BN) || !make_map(&mGVr, gv, p, R::BN))
+  if (!make_map(&mQr, q, p, R::BM) || !make_map(&mGQr, has_gq ? gq : q, p, R::BM) ||
+      !make_map(&mKr, k, p, R::BN, true) || !make_map(&mGKr, has_gk ? gk : k, p, R::BN, true) ||
+      !make_map(&mVr, v, p, R::BN) || !make_map(&mGVr, has_gv ? gv : v, p, R::BN))
     return cudaErrorInvalidValue;
   CUtensorMap mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc;
-  if (!make_map(&mKc, k, p, Cc::BM) || !make_map(&mGKc, gk, p, Cc::BM) ||
-      !make_map(&mVc, v, p, Cc::BM) || !make_map(&mGVc, gv, p, Cc::BM) ||
-      !make_map(&mQc, q, p, Cc::BN, true) || !make_map(&mGQc, gq, p, Cc::BN, true) ||
+  if (!make_map(&mKc, k, p, Cc::BM) || !make_map(&mGKc, has_gk ? gk : k, p, Cc::BM) ||
+      !make_map(&mVc, v, p, Cc::BM) || !make_map(&mGVc, has_gv ? gv : v, p, Cc::BM) ||
+      !make_map(&mQc, q, p, Cc::BN, true) || !make_map(&mGQc, has_gq ? gq : q, p, Cc::BN, true) ||
       !make_map(&mDOc, dO, p, Cc::BN))
     return cudaErrorInvalidValue;
 
-  cudaError_t e = cudaFuncSetAttribute(bob_row_pass<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool all = has_gq && has_gk && has_gv;
+  auto row_kernel = all ? bob_row_pass<D, true> : bob_row_pass<D, false>;
+  auto col_kernel = all ? bob_col_pass<D, true> : bob_col_pass<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)R::SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bob_col_pass<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(col_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)Cc::SMEM);
   if (e != cudaSuccess) return e;
 
@@ -909,8 +963,11 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
   rp.N = p.N;
   rp.causal = p.causal;
   rp.scale = p.scale;
+  rp.has_gq = has_gq;
+  rp.has_gk = has_gk;
+  rp.has_gv = has_gv;
   dim3 g1((p.N + R::BM - 1) / R::BM, p.BH());
-  bob_row_pass<D><<<g1, kThreads, R::SMEM, log.stream>>>(mQr, mGQr, mKr, mGKr, mVr, mGVr, rp);
+  row_kernel<<<g1, kThreads, R::SMEM, log.stream>>>(mQr, mGQr, mKr, mGKr, mVr, mGVr, rp);
   e = cudaGetLastError();
   log.mark();
   if (e != cudaSuccess) return e;
@@ -927,8 +984,11 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
   cp.N = p.N;
   cp.causal = p.causal;
   cp.scale = p.scale;
+  cp.has_gq = has_gq;
+  cp.has_gk = has_gk;
+  cp.has_gv = has_gv;
   dim3 g2((p.N + Cc::BM - 1) / Cc::BM, p.BH());
-  bob_col_pass<D><<<g2, kColThreads, Cc::SMEM, log.stream>>>(mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc, cp);
+  col_kernel<<<g2, kColThreads, Cc::SMEM, log.stream>>>(mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc, cp);
   e = cudaGetLastError();
   log.mark();
   if (e != cudaSuccess) return e;

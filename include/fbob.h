@@ -107,6 +107,9 @@ int fbob_backward(const fbob_shape_t* shape, const void* q, const void* k,
  *   q, k, v, o, dO, gq, gk, gv : [B,H,N,d] inputs
  *   lse                        : [B,H,N] fp32 from fbob_forward
  *   gradq, gradk, gradv, graddo: [B,H,N,d] outputs (fully overwritten)
+ * Any of gq, gk, gv may be NULL: that cotangent is zero (a loss that reads
+ * only some of dQ, dK, dV).  The kernels then skip its loads and the MMAs
+ * it feeds.  With all three NULL, L = 0 and the four outputs are zeroed.
  * Exact BoB, "FlashBoB: I/O-Efficient Exact Backward-over-Backward for
  * Softmax Attention", Abstract: two row-wise scalars per query (r and sigma,
  * reduced in a row-stationary pass) determine every output through affine

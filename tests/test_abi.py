@@ -98,6 +98,23 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.fbob_forward(None, good, good, good, good, good, good, 1 << 20, None) == 1
 
 
+def test_null_cotangents_are_accepted_misaligned_ones_rejected(lib):
+    """gq, gk, gv (arguments 6-8) may be NULL (zero cotangents); a present
+    one must still be 16-byte aligned.  The workspace given is too small, so
+    an accepted call stops at FBOB_ERR_WORKSPACE before touching a device."""
+    s = shape()
+    good = ctypes.c_void_p(1 << 20)
+    for nulls in ((6,), (7,), (8,), (6, 7), (6, 8), (7, 8), (6, 7, 8)):
+        args = [good] * 13
+        for i in nulls:
+            args[i] = None
+        assert lib.fbob_bob(ctypes.byref(s), *args, good, 16, None) == 3, nulls
+    args = [good] * 13
+    args[6] = None
+    args[7] = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.fbob_bob(ctypes.byref(s), *args, good, 16, None) == 1
+
+
 def test_kernel_family_choice(lib):
     """bf16 at d = 64 / 128 takes the tcgen05 kernels for all three calls;
     fp32 and other head sizes take the CUDA-core kernels."""

@@ -155,3 +155,43 @@ def test_workload_peaked_n65536_d128_sampled():
 def test_workload_n262144_d64_sampled():
     w = WORKLOADS["bf16_causal_h4_n262144_d64"]
     sampled_check(w, n_rows=12, n_tail=32, heads=((0, 1),))
+
+
+# ------------------------------------------------- optional cotangents ---
+
+SUBSETS = [("gq",), ("gk",), ("gv",), ("gq", "gk"), ("gq", "gv"), ("gk", "gv")]
+
+
+@pytest.mark.parametrize("present", SUBSETS, ids=["+".join(p) for p in SUBSETS])
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (128, "bf16"), (40, "fp32")],
+                         ids=["d64_tc", "d128_tc", "d40_simt"])
+def test_absent_cotangents_are_zero(present, d, dtype):
+    """gq / gk / gv passed as None (NULL in the C ABI): the result equals BoB
+    with those cotangents zero, on both kernel families."""
+    w = Workload("opt", 1, 2, 193, d, dtype, True, 1.0, 1.0, 0.3)
+    ins = make(w, 11)
+    x = {k: to64(v) for k, v in ins.items()}
+    zero = np.zeros_like(x["gq"])
+    cot = {n: (x[n] if n in present else zero) for n in ("gq", "gk", "gv")}
+    ref = oracle.bob_batched(x["q"], x["k"], x["v"], x["do"], cot["gq"], cot["gk"], cot["gv"],
+                             True, w.scale)
+    dev = {k: v.cuda() for k, v in ins.items()}
+    o, lse = fbob.forward(dev["q"], dev["k"], dev["v"], True, w.scale)
+    got = fbob.bob(dev["q"], dev["k"], dev["v"], o, lse, dev["do"],
+                   *(dev[n] if n in present else None for n in ("gq", "gk", "gv")),
+                   True, w.scale)
+    floor = 0.1 * max(float(np.max(np.abs(r))) for r in ref)
+    tol = tol_for(w)
+    errs = [rel_err(to64(g), r, floor=floor) for g, r in zip(got, ref)]
+    assert max(errs) <= tol, (present, errs)
+
+
+def test_all_cotangents_absent_gives_zeros():
+    w = Workload("none", 1, 1, 70, 64, "bf16", True, 1.0, 1.0, 0.3)
+    dev = {k: v.cuda() for k, v in make(w, 2).items()}
+    o, lse = fbob.forward(dev["q"], dev["k"], dev["v"], True, w.scale)
+    outs = tuple(torch.full_like(dev["q"], float("nan")) for _ in range(4))
+    got = fbob.bob(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], None, None, None, True,
+                   w.scale, out=outs)
+    for g in got:
+        assert torch.count_nonzero(g).item() == 0
