@@ -347,39 +347,62 @@ def run_ours(args, w, rank, world, dist):
 
 
 def run_e2e(args, w, host, o, lse, outs, ws, call_api, dev):
-    """Same metric through the public API: every step copies the inputs from
-    pinned host memory and reads the four results back."""
+    """Same metric through the public API: every step copies its inputs from
+    pinned host memory and reads its four results back.  Steps are
+    pipelined over three streams with two sets of device buffers: the
+    host->device copy of step i+1 and the device->host read of step i-1 run
+    on their own streams while step i computes."""
     import torch
     names = ("q", "k", "v", "do", "gq", "gk", "gv")
     h_in = {n: host[n].pin_memory() for n in names}
     h_in["o"] = o.cpu().pin_memory()
     h_in["lse"] = lse.cpu().pin_memory()
-    d_in = {n: torch.empty_like(h_in[n], device=dev) for n in h_in}
     h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out)
+    nbuf = 2
+    d_in = [{n: torch.empty_like(h_in[n], device=dev) for n in h_in} for _ in range(nbuf)]
+    d_out = [outs] + [tuple(torch.empty_like(t) for t in outs) for _ in range(nbuf - 1)]
+    s_h2d, s_cmp, s_d2h = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]    # inputs of buffer b landed
+    ev_done = [torch.cuda.Event() for _ in range(nbuf)]  # step on buffer b computed
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]   # results of buffer b read back
 
-    def step():
-        for n in h_in:
-            d_in[n].copy_(h_in[n], non_blocking=True)
-        res = call_api(d_in["q"], d_in["k"], d_in["v"], d_in["o"], d_in["lse"], d_in["do"],
-                       d_in["gq"], d_in["gk"], d_in["gv"], w.causal, w.scale, out=outs,
-                       workspace=ws)
-        for h, d in zip(h_out, res):
-            h.copy_(d, non_blocking=True)
+    def step(i):
+        b = i % nbuf
+        with torch.cuda.stream(s_h2d):
+            s_h2d.wait_event(ev_done[b])        # the step that last read buffer b is done
+            for n in h_in:
+                d_in[b][n].copy_(h_in[n], non_blocking=True)
+            ev_in[b].record(s_h2d)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev_in[b])
+            s_cmp.wait_event(ev_out[b])          # results of buffer b were read back
+            call_api(d_in[b]["q"], d_in[b]["k"], d_in[b]["v"], d_in[b]["o"], d_in[b]["lse"],
+                     d_in[b]["do"], d_in[b]["gq"], d_in[b]["gk"], d_in[b]["gv"], w.causal,
+                     w.scale, out=d_out[b], workspace=ws)
+            ev_done[b].record(s_cmp)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev_done[b])
+            for h, d in zip(h_out, d_out[b]):
+                h.copy_(d, non_blocking=True)
+            ev_out[b].record(s_d2h)
 
     steps = max(2, min(args.steps, args.e2e_steps))
-    step()
+    for i in range(nbuf):
+        step(i)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        step()
-    b.record()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_h2d)
+    for i in range(steps):
+        step(i)
+    s_h2d.wait_stream(s_d2h)  # the end event follows the last read-back
+    e.record(s_h2d)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
+    ms = a.elapsed_time(e) / steps
     return {"value": flops_bob(w) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
-            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": "h2d / compute / d2h streams, 2 buffer sets"}
 
 
 def main(argv=None):
@@ -390,7 +413,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

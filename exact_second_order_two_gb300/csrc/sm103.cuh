@@ -221,6 +221,16 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t t0, uint32_t t1, uint32_t (
       : "memory");
 }
 
+// 32 lanes x 8 columns, with its completion wait.
+__device__ __forceinline__ void tmem_st8(uint32_t ta, const uint32_t (&a)[8]) {
+  __syncwarp();
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(ta),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
+      : "memory");
+}
+
 // Two 8-column stores (32 lanes x 8 words each) and one completion wait.
 __device__ __forceinline__ void tmem_st8x2(uint32_t ta, const uint32_t (&a)[8], uint32_t tb,
                                            const uint32_t (&b)[8]) {

@@ -38,11 +38,16 @@ using namespace tc;
 
 namespace {
 
-constexpr int kFwdConsumerWarps = 8;
+// Forward warp roles: warps 0-15 elementwise (warp w: TMEM lane quadrant
+// w % 4, 16-key slice w / 4 of the 64-key tile), warp 16 TMA producer,
+// warp 17 TMEM allocator and MMA issuer.
+constexpr int kFwdConsumerWarps = 16;
 constexpr int kFwdConsumers = kFwdConsumerWarps * 32;
-constexpr int kFwdProducerWarp = 8;
-constexpr int kFwdMmaWarp = 9;
-constexpr int kFwdThreads = 320;
+constexpr int kFwdProducerWarp = kFwdConsumerWarps;
+constexpr int kFwdMmaWarp = kFwdConsumerWarps + 1;
+constexpr int kFwdThreads = (kFwdConsumerWarps + 2) * 32;
+constexpr int kFwdSlices = kFwdConsumerWarps / 4;  // column slices per row
+constexpr int kFwdCols = 64 / kFwdSlices;           // key columns per thread
 constexpr float kLn2 = 0.6931471805599453f;
 
 // ===========================================================================
@@ -55,8 +60,8 @@ struct Fwd {
   static constexpr uint32_t QB = BM * D * 2;   // stationary Q tile
   static constexpr uint32_t KB = BN * D * 2;   // one streamed K or V tile
   static constexpr uint32_t OFF_Q = 0, OFF_K = QB, OFF_V = OFF_K + KSTAGES * KB;
-  static constexpr uint32_t OFF_PART = OFF_V + VSTAGES * KB;    // [2 halves][m, l][128]
-  static constexpr uint32_t OFF_MISC = OFF_PART + 4 * 128 * 4;  // barriers, slot, flag
+  static constexpr uint32_t OFF_PART = OFF_V + VSTAGES * KB;  // [m, l][slices][128]
+  static constexpr uint32_t OFF_MISC = OFF_PART + 2 * kFwdSlices * 128 * 4;
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "forward shared memory budget");
@@ -225,8 +230,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else {
     // ---------------- elementwise warps: thread = query row --------------
+    constexpr int NC = kFwdCols, NS = kFwdSlices;
     const int row = 32 * (warp & 3) + lane;
-    const int half = warp >> 2;  // columns [32*half, 32*half + 32) of a key tile
+    const int slice = warp >> 2;  // key columns [NC*slice, NC*slice + NC) of a tile
     const int i = i0 + row;
     const bool row_ok = i < N;
     const size_t srow = (size_t)bh * N + (row_ok ? i : 0);
@@ -235,9 +241,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool ok = warp_wait(q_full, 0, abort_flag, prm.status);
     if (ok) {
       // stationary Q row -> TMEM (bf16 pairs, lower half = even feature): one
-      // 64-feature half-row per thread (d = 64: the first warp group only)
-      if (half < D / 64) {
-        const uint32_t src = C::OFF_Q + half * C::BM * 128 + row * 128;
+      // 64-feature half-row per thread of slices 0 .. D/64 - 1
+      if (slice < D / 64) {
+        const uint32_t src = C::OFF_Q + slice * C::BM * 128 + row * 128;
         uint32_t lo[16], hi[16];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           uint32_t* dst = c < 4 ? lo + 4 * c : hi + 4 * (c - 4);
           dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
         }
-        const uint32_t dst = tmem + lane_off + C::T_QA + 32 * half;
+        const uint32_t dst = tmem + lane_off + C::T_QA + 32 * slice;
         tmem_st16(dst, lo);
         tmem_st16(dst + 16, hi);
       }
@@ -256,23 +262,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     float m2 = -INFINITY, l = 0.f;
     // S of iteration it (sweep 1: it < T, sweep 2: it >= T) into registers;
     // false if a wait gave up
-    auto load_s = [&](int it, uint32_t (&sr)[32]) -> bool {
+    auto load_s = [&](int it, uint32_t (&sr)[NC]) -> bool {
       const int b = it & 1;
       if (!warp_wait(s_full + b, (it >> 1) & 1, abort_flag, prm.status)) return false;
       tc_fence_after();
-      tmem_ld32(tmem + lane_off + C::T_S(b) + 32 * half, sr);
+      tmem_ld16(tmem + lane_off + C::T_S(b) + NC * slice, sr);
       tc_fence_before();
       mbar_arrive(s_empty + b);
       return true;
     };
     for (int t = 0; ok && t < T; ++t) {
-      uint32_t sr[32];
+      uint32_t sr[NC];
       if (!load_s(t, sr)) { ok = false; break; }
-      const int j0 = rotated(t, rot, T) * C::BN + 32 * half;
-      const bool need_mask = !row_ok || (j0 + 32 > N) || (prm.causal && j0 + 31 > i);
+      const int j0 = rotated(t, rot, T) * C::BN + NC * slice;
+      const bool need_mask = !row_ok || (j0 + NC > N) || (prm.causal && j0 + NC - 1 > i);
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < NC; ++c) {
         const int j = j0 + c;
         const bool in = !need_mask || (row_ok && j < N && (!prm.causal || j <= i));
         mx = in ? fmaxf(mx, __uint_as_float(sr[c]) * sc2) : mx;
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (m2 > -INFINITY) {
         float acc = 0.f;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < NC; ++c) {
           const int j = j0 + c;
           const bool in = !need_mask || (row_ok && j < N && (!prm.causal || j <= i));
           const float e = ex2_approx(__uint_as_float(sr[c]) * sc2 - m2);
@@ -293,28 +299,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         l += acc;
       }
     }
-    // combine the two column halves of each row (every consumer thread gets
-    // here, also after a failed wait, so the barrier cannot hang)
-    part[half * 128 + row] = m2;
-    part[256 + half * 128 + row] = l;
+    // combine the column slices of each row (every consumer thread gets here,
+    // also after a failed wait, so the barrier cannot hang)
+    part[slice * 128 + row] = m2;
+    part[(NS + slice) * 128 + row] = l;
     named_sync<kFwdConsumers>(1);
     float lse2;
     {
-      const float ma = part[row], mb = part[128 + row];
-      const float M = fmaxf(ma, mb);
-      const float L = (ma > -INFINITY ? part[256 + row] * ex2_approx(ma - M) : 0.f) +
-                      (mb > -INFINITY ? part[384 + row] * ex2_approx(mb - M) : 0.f);
+      float M = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < NS; ++u) M = fmaxf(M, part[u * 128 + row]);
+      float L = 0.f;
+#pragma unroll
+      for (int u = 0; u < NS; ++u) {
+        const float mu = part[u * 128 + row];
+        L += mu > -INFINITY ? part[(NS + u) * 128 + row] * ex2_approx(mu - M) : 0.f;
+      }
       lse2 = (M > -INFINITY && L > 0.f) ? M + log2f(L) : 0.f;
     }
     for (int t = 0; ok && t < T; ++t) {
-      uint32_t sr[32];
+      uint32_t sr[NC];
       if (!load_s(T + t, sr)) { ok = false; break; }
-      const int j0 = rotated(t, rot, T) * C::BN + 32 * half;
-      const bool need_mask = !row_ok || (j0 + 32 > N) || (prm.causal && j0 + 31 > i);
-      uint32_t pw[16];
+      const int j0 = rotated(t, rot, T) * C::BN + NC * slice;
+      const bool need_mask = !row_ok || (j0 + NC > N) || (prm.causal && j0 + NC - 1 > i);
+      uint32_t pw[NC / 2];
       auto body = [&](auto masked) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
+        for (int c = 0; c < NC; c += 2) {
           float p0 = ex2_approx(__uint_as_float(sr[c]) * sc2 - lse2);
           float p1 = ex2_approx(__uint_as_float(sr[c + 1]) * sc2 - lse2);
           if (decltype(masked)::value) {
@@ -329,7 +340,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         body(std::true_type{});
       else
         body(std::false_type{});
-      keep16(pw);
       const int pb = t & 1;
       // P buffer pb was last read by the O MMAs of tile t-2
       if (t >= 2 && !warp_wait(p_empty + pb, ((t >> 1) - 1) & 1, abort_flag, prm.status)) {
@@ -337,7 +347,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         break;
       }
       tc_fence_after();
-      tmem_st16(tmem + lane_off + C::T_P(pb) + 16 * half, pw);
+      // keys NC*slice + 2c, + 1 in column NC/2*slice + c: one 16-key MMA step
+      tmem_st8(tmem + lane_off + C::T_P(pb) + (NC / 2) * slice, pw);
       tc_fence_before();
       mbar_arrive(p_full + pb);
     }
@@ -346,12 +357,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (ok) ok = warp_wait(o_done, 0, abort_flag, prm.status);
     tc_fence_after();
     if (ok) {
-      constexpr int HALF = D / 2;
-      uint4* op = reinterpret_cast<uint4*>(prm.o + srow * D + HALF * half);
+      constexpr int PART = D / NS;  // output features per thread
+      uint4* op = reinterpret_cast<uint4*>(prm.o + srow * D + PART * slice);
 #pragma unroll
-      for (int cc = 0; cc < HALF; cc += 16) {
+      for (int cc = 0; cc < PART; cc += 16) {
         uint32_t v[16];
-        tmem_ld16(tmem + lane_off + C::T_O + HALF * half + cc, v);
+        tmem_ld16(tmem + lane_off + C::T_O + PART * slice + cc, v);
         if (row_ok) {
 #pragma unroll
           for (int q = 0; q < 2; ++q)
@@ -362,7 +373,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
         }
       }
-      if (half == 0 && row_ok) prm.lse[srow] = lse2 * kLn2;
+      if (slice == 0 && row_ok) prm.lse[srow] = lse2 * kLn2;
     }
   }
   tc_fence_before();
