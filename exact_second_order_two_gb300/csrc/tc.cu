@@ -53,8 +53,11 @@ constexpr int kThreads = 320;
 constexpr int kConsumers = kConsumerWarps * 32;
 __device__ __forceinline__ void consumer_sync() { named_sync<kConsumers>(1); }
 
-// [K|gK] (or [Q|gQ]) pair stage: the second tensor is skipped when its
-// cotangent is absent (the MMAs then read only the first BN rows per half).
+// Two [rows][D] tiles A and B interleaved per 64-feature half (A_h, B_h,
+// A_h+1, ...): each half holds 2*rows rows, so one N = 2*rows MMA sees A and B
+// stacked; maps with one feature half per box.  B ([K|gK] or [Q|gQ] with gK /
+// gQ as B) is skipped when its cotangent is absent: the MMAs then read only
+// the first `rows` rows of each half.
 template <int D>
 __device__ __forceinline__ void load_pair_opt(uint8_t* dst, const CUtensorMap* mapA,
                                               const CUtensorMap* mapB, bool with_b, uint64_t* bar,

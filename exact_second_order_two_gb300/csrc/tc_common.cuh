@@ -70,20 +70,6 @@ __device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, uin
   tma_load_4d(dst, map, bar, 0, row, 0, bh);
 }
 
-// Two [rows][D] tiles A and B interleaved per 64-feature half (A_h, B_h,
-// A_h+1, ...): each half holds 2*rows rows, so one N = 2*rows MMA sees A and B
-// stacked.  Maps with one feature half per box.
-template <int D>
-__device__ __forceinline__ void load_pair(uint8_t* dst, const CUtensorMap* mapA,
-                                          const CUtensorMap* mapB, uint64_t* bar, int rows, int row,
-                                          int bh) {
-#pragma unroll
-  for (int h = 0; h < D / 64; ++h) {
-    tma_load_4d(dst + h * 2 * rows * 128, mapA, bar, 0, row, h, bh);
-    tma_load_4d(dst + h * 2 * rows * 128 + rows * 128, mapB, bar, 0, row, h, bh);
-  }
-}
-
 // K-major tile [rows][D] stored as D/64 boxes of [rows][64] (128 B rows,
 // 128-byte swizzle): offset of the k-th 16-element slice along D, in
 // descriptor units (16 bytes), to add to the tile's descriptor low word.

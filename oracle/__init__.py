@@ -2,6 +2,8 @@
 from .attention_oracle import (  # noqa: F401
     backward,
     backward_batched,
+    backward_cols,
+    backward_rows,
     bob,
     bob_batched,
     bob_cols,
@@ -9,4 +11,5 @@ from .attention_oracle import (  # noqa: F401
     default_row_block,
     forward,
     forward_batched,
+    forward_rows,
 )

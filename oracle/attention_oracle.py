@@ -133,6 +133,49 @@ def backward(q, k, v, do, causal: bool, scale: float,
     return dq, dk, dv
 
 
+def forward_rows(q, k, v, causal: bool, scale: float, rows):
+    """O and LSE at the query rows ``rows`` only (row-local, so large-N
+    sampling costs O(len(rows) * N * d)); same definition as ``forward``."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    rows = np.asarray(rows, dtype=np.int64)
+    _, _, o, lse = _row_block_forward(q, k, v, rows, causal, scale)
+    return o, lse
+
+
+def backward_rows(q, k, v, do, causal: bool, scale: float, rows):
+    """dQ at the query rows ``rows`` only: row i of dS needs row i of P and
+    D_i alone, so this is row-local; same definition as ``backward``."""
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    rows = np.asarray(rows, dtype=np.int64)
+    _, p, o, _ = _row_block_forward(q, k, v, rows, causal, scale)
+    dp = do[rows] @ v.T
+    dd = np.sum(do[rows] * o, axis=1, keepdims=True)
+    return scale * ((p * (dp - dd)) @ k)
+
+
+def backward_cols(q, k, v, do, causal: bool, scale: float, cols,
+                  row_block: int | None = None):
+    """dK and dV at the key rows ``cols`` only: column j sums over every
+    query row that sees key j (rows i >= min(cols) when causal); same
+    definition as ``backward``."""
+    q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
+    cols = np.asarray(cols, dtype=np.int64)
+    n = q.shape[0]
+    rb = row_block or default_row_block(n)
+    first = int(cols.min()) if causal else 0
+    dk = np.zeros((cols.size, k.shape[1]))
+    dv = np.zeros((cols.size, v.shape[1]))
+    for r0 in range(first, n, rb):
+        rows = np.arange(r0, min(n, r0 + rb))
+        _, p, o, _ = _row_block_forward(q, k, v, rows, causal, scale)
+        dp = do[rows] @ v[cols].T
+        dd = np.sum(do[rows] * o, axis=1, keepdims=True)
+        ds = p[:, cols] * (dp - dd)
+        dk += scale * (ds.T @ q[rows])
+        dv += p[:, cols].T @ do[rows]
+    return dk, dv
+
+
 # --------------------------------------------------------------------------
 # backward-over-backward
 # --------------------------------------------------------------------------

@@ -125,13 +125,26 @@ def sampled_check(w: Workload, n_rows=24, n_tail=128, heads=((0, 0),), seed=0):
                 w.causal, w.scale)
         gq_r, gdo_r = oracle.bob_rows(*args, rows)
         gk_c, gv_c = oracle.bob_cols(*args, cols)
+        # the forward and first backward that produced BoB's inputs, sampled
+        # the same way
+        fb = (x["q"], x["k"], x["v"])
+        o_r, lse_r = oracle.forward_rows(*fb, w.causal, w.scale, rows)
+        dq_r = oracle.backward_rows(*fb, x["do"], w.causal, w.scale, rows)
+        dk_c, dv_c = oracle.backward_cols(*fb, x["do"], w.causal, w.scale, cols)
         got = {"gradq": to64(gpu["gradq"][b, h])[rows],
                "graddo": to64(gpu["graddo"][b, h])[rows],
                "gradk": to64(gpu["gradk"][b, h])[cols],
-               "gradv": to64(gpu["gradv"][b, h])[cols]}
-        ref = {"gradq": gq_r, "graddo": gdo_r, "gradk": gk_c, "gradv": gv_c}
+               "gradv": to64(gpu["gradv"][b, h])[cols],
+               "o": to64(gpu["o"][b, h])[rows],
+               "dq": to64(gpu["dq"][b, h])[rows],
+               "dk": to64(gpu["dk"][b, h])[cols],
+               "dv": to64(gpu["dv"][b, h])[cols]}
+        ref = {"gradq": gq_r, "graddo": gdo_r, "gradk": gk_c, "gradv": gv_c,
+               "o": o_r, "dq": dq_r, "dk": dk_c, "dv": dv_c}
         errs = {k: rel_err(got[k], ref[k]) for k in got}
         assert all(e <= tol for e in errs.values()), (w.name, b, h, errs)
+        lse_err = float(np.max(np.abs(to64(gpu["lse"][b, h])[rows] - lse_r)))
+        assert lse_err <= 1e-2, (w.name, b, h, lse_err)
     for k in ("gradq", "gradk", "gradv", "graddo"):
         assert torch.isfinite(gpu[k].float()).all(), k
     res = invariant_residuals(gpu)

@@ -292,6 +292,26 @@ def test_bob_row_blocking_and_sampling_agree(causal):
     assert np.max(np.abs(gv_c - ref[2][cols])) < 1e-12
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_backward_sampling_agrees_with_full(causal):
+    """The sampled forward / first-backward oracles (rows of O, LSE, dQ;
+    columns of dK, dV) reproduce the full ones, whose own pins are the
+    brute-force loops and finite differences above."""
+    n, d, scale = 41, 5, 0.6
+    q, k, v, do = rnd(21, n, d, 4)
+    o, lse = oracle.forward(q, k, v, causal, scale)
+    dq, dk, dv = oracle.backward(q, k, v, do, causal, scale)
+    rows = np.array([0, 1, 17, 40])
+    o_r, lse_r = oracle.forward_rows(q, k, v, causal, scale, rows)
+    assert np.max(np.abs(o_r - o[rows])) < 1e-12
+    assert np.max(np.abs(lse_r - lse[rows])) < 1e-12
+    assert np.max(np.abs(oracle.backward_rows(q, k, v, do, causal, scale, rows) - dq[rows])) < 1e-12
+    cols = np.array([39, 2, 40, 23])
+    dk_c, dv_c = oracle.backward_cols(q, k, v, do, causal, scale, cols, row_block=6)
+    assert np.max(np.abs(dk_c - dk[cols])) < 1e-12
+    assert np.max(np.abs(dv_c - dv[cols])) < 1e-12
+
+
 def test_batched_wrappers_match_per_head():
     B, H, n, d = 2, 3, 9, 4
     rng = np.random.default_rng(14)
