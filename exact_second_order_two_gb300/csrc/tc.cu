@@ -246,17 +246,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
+    {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);    // gQ K^T: M=128 N=64
       constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // Q [K;gK]^T: N=128
       constexpr uint32_t id_w = idesc_bf16(128, D, false, true);    // W: N=D, B MN-major
-      bool ok = wait_bar(q_tmem, 0, abort_flag, prm.status);
+      bool ok = warp_wait(q_tmem, 0, abort_flag, prm.status);
       const uint32_t tw = tmem + C::T_W, tq = tmem + C::T_QA, tgq = tmem + C::T_GQA;
       // S and G of tile t into buffer t & 1
-      auto issue_sg = [&](int t) -> bool {
+      // waits and issue are split so that one tile's waits all come before
+      // its MMAs: a wait right after a burst of MMA issue costs hundreds of
+      // cycles even on a completed barrier
+      auto wait_sg = [&](int t) -> bool {
+        return warp_wait(kg_full + t % C::STAGES, (t / C::STAGES) & 1, abort_flag, prm.status);
+      };
+      auto wait_w = [&](int t) -> bool {
+        return warp_wait(p_full + (t & 1), (t >> 1) & 1, abort_flag, prm.status) &&
+               warp_wait(v_full + t % C::VSTAGES, (t / C::VSTAGES) & 1, abort_flag, prm.status);
+      };
+      auto issue_sg = [&](int t) {
         const int s = t % C::STAGES, b = t & 1;
-        if (!wait_bar(kg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
-        tc_fence_after();
         // [K;gK] per half, 2*BN rows
         const uint32_t kgk_lo = opaque(lo_kmajor(sb + C::OFF_KG + s * C::SB));
         const uint32_t ts = tmem + C::T_S(b), tg = tmem + C::T_G(b);
@@ -265,24 +273,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id_first = has_gk ? id_sg : id_s;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ts(ts, tq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_first, k > 0 ? 1u : 0u);
+          mma_ts_w(ts, tq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_first, k > 0 ? 1u : 0u);
         // G += gQ K^T (the first BN rows of each [K;gK] half are K), A = gQ from TMEM
         if (has_gq) {
           const uint32_t g0 = has_gk ? 1u : 0u;  // without gK this starts G
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            mma_ts(tg, tgq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_s, k > 0 ? 1u : g0);
+            mma_ts_w(tg, tgq + 8 * k, kgk_lo + kslice_off(2 * C::BN, k), id_s, k > 0 ? 1u : g0);
         }
-        mma_commit(sg_full + b);
-        mma_commit(kg_empty + s);
-        return true;
+        mma_commit_w(sg_full + b);
+        mma_commit_w(kg_empty + s);
       };
       // W += P gV + (P*G) V for tile t: A operands (bf16 P, P*G) from TMEM
-      auto issue_w = [&](int t) -> bool {
+      auto issue_w = [&](int t) {
         const int s = t % C::VSTAGES, b = t & 1;
-        if (!wait_bar(p_full + b, (t >> 1) & 1, abort_flag, prm.status)) return false;
-        if (!wait_bar(v_full + s, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
-        tc_fence_after();
         const uint32_t st = sb + C::OFF_V + s * C::SB;
         const uint32_t v_lo = opaque(lo_mnmajor(st, C::BN * 128)),
                        gv_lo = opaque(lo_mnmajor(st + C::KB, C::BN * 128));
@@ -293,23 +297,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 keys
           const uint32_t acc = k > 0 ? 1u : first;
-          if (use_gv) mma_ts(tw, tp + C::p_col(k), gv_lo + kstep_off(k), id_w, acc);
-          if (use_g) mma_ts(tw, tpg + C::p_col(k), v_lo + kstep_off(k), id_w, use_gv ? 1u : acc);
+          if (use_gv) mma_ts_w(tw, tp + C::p_col(k), gv_lo + kstep_off(k), id_w, acc);
+          if (use_g) mma_ts_w(tw, tpg + C::p_col(k), v_lo + kstep_off(k), id_w, use_gv ? 1u : acc);
         }
-        mma_commit(v_empty + s);
-        return true;
+        mma_commit_w(v_empty + s);
       };
       // Buffer b holds tile t until the W MMAs of t have read its P: the S/G
       // MMAs of tile t + 2 are issued after them, and MMAs from one thread
       // run in issue order.
-      ok = ok && issue_sg(0) && (T < 2 || issue_sg(1));
-      for (int t = 0; ok && t < T; ++t) {
-        if (!issue_w(t)) { ok = false; break; }
-        if (t + 2 < T && !issue_sg(t + 2)) { ok = false; break; }
+      for (int t = 0; ok && t < 2 && t < T; ++t) {
+        ok = wait_sg(t);
+        if (ok) {
+          tc_fence_after();
+          issue_sg(t);
+        }
       }
-      if (ok) mma_commit(w_done);
+      for (int t = 0; ok && t < T; ++t) {
+        ok = wait_w(t) && (t + 2 >= T || wait_sg(t + 2));
+        if (!ok) break;
+        tc_fence_after();
+        issue_w(t);
+        if (t + 2 < T) issue_sg(t + 2);
+      }
+      if (ok) mma_commit_w(w_done);
       // every MMA this thread issued has completed before TMEM is released
-      mma_commit(drain);
+      mma_commit_w(drain);
       mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
     }
   } else {
@@ -665,7 +677,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
       }
     }
   } else if (warp == kColMmaWarp) {
-    if (lane == 0) {
+    {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
       constexpr uint32_t id_sc = idesc_bf16(128, 64, false, false);  // scores: M=128 N=64
       constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // K [Q;gQ]^T: N=128
       constexpr uint32_t id_out = idesc_bf16(128, D, false, true);   // gradK/V: N=D, B MN
@@ -687,19 +699,19 @@ __global__ void __launch_bounds__(kColThreads, 1)
         const uint32_t qgq_lo = opaque(lo_kmajor(sb + C::OFF_QG + s * 2 * C::QB));  // [Q;gQ] per half
         const uint32_t v_l = opaque(v_lo), gv_l = opaque(gv_lo), k_l = opaque(k_lo),
                        gk_l = opaque(gk_lo);
-        if (!wait_bar(do_full + ds, (t / C::DSTAGES) & 1, abort_flag, prm.status)) return false;
+        if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc, k > 0 ? 1u : 0u);
+          mma_ss_w(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc, k > 0 ? 1u : 0u);
         if (has_gv) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            mma_ss(t_h, gv_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
+            mma_ss_w(t_h, gv_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
                    k > 0 ? 1u : 0u);
         }
-        if (!wait_bar(qg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
-        if (C::GQ_IN_S && t >= 1 && !wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status))
+        if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
+        if (C::GQ_IN_S && t >= 1 && !warp_wait(gq_empty, (t - 1) & 1, abort_flag, prm.status))
           return false;
         tc_fence_after();
         // [S^T | K gQ^T] = K [Q; gQ]^T (S^T = K Q^T alone without gQ), then
@@ -707,19 +719,19 @@ __global__ void __launch_bounds__(kColThreads, 1)
         const uint32_t id_first = has_gq ? id_sg : id_sc;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(t_s, k_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_first,
+          mma_ss_w(t_s, k_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_first,
                  k > 0 ? 1u : 0u);
         if (has_gk) {
           const uint32_t g0 = has_gq ? 1u : 0u;  // without gQ this starts G^T
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            mma_ss(t_g, gk_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_sc,
+            mma_ss_w(t_g, gk_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_sc,
                    k > 0 ? 1u : g0);
         }
-        mma_commit(sc_full);
+        mma_commit_w(sc_full);
         return true;
       };
-      bool ok = wait_bar(kv_full, 0, abort_flag, prm.status) && issue_scores(0);
+      bool ok = warp_wait(kv_full, 0, abort_flag, prm.status) && issue_scores(0);
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES, ds = t % C::DSTAGES;
         const uint32_t qgq_s = sb + C::OFF_QG + s * 2 * C::QB;
@@ -732,35 +744,35 @@ __global__ void __launch_bounds__(kColThreads, 1)
                        gs_m = opaque(gs_mn);
         const uint32_t first = t > 0 ? 1u : 0u;
         // ---- outputs: A operands (bf16 gS^T, dS^T, gdP^T) from TMEM ----
-        if (!wait_bar(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (!warp_wait(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
         // gradK first: it releases the [Q|gQ] stage that the next tile waits for
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 queries
-          mma_ts(t_gk, t_g + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-          if (has_gq) mma_ts(t_gk, t_dp + 16 * k, gq_mn + kstep_off(k), id_out, 1u);
+          mma_ts_w(t_gk, t_g + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+          if (has_gq) mma_ts_w(t_gk, t_dp + 16 * k, gq_mn + kstep_off(k), id_out, 1u);
         }
-        mma_commit(qg_empty + s);
+        mma_commit_w(qg_empty + s);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts(t_gv, t_h + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-        mma_commit(do_empty + ds);
+          mma_ts_w(t_gv, t_h + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+        mma_commit_w(do_empty + ds);
         if (!C::GQ_IN_S && t >= 1) {
-          if (!wait_bar(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+          if (!warp_wait(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
           tc_fence_after();
         }
 #pragma unroll
         for (int k = 0; k < C::BM / 16; ++k) {  // contraction over the 128 keys
-          mma_ss(t_gq, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
-          if (has_gk) mma_ss(t_gq, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
+          mma_ss_w(t_gq, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
+          if (has_gk) mma_ss_w(t_gq, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
         }
-        mma_commit(gq_full);
+        mma_commit_w(gq_full);
         // the next tile's scores overwrite the A operands read above; MMAs
         // from one thread run in issue order
         if (t + 1 < T && !issue_scores(t + 1)) { ok = false; break; }
       }
-      if (ok) mma_commit(acc_done);
-      mma_commit(drain);
+      if (ok) mma_commit_w(acc_done);
+      mma_commit_w(drain);
       mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
     }
   } else {

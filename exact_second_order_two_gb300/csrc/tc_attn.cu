@@ -189,43 +189,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     }
   } else if (warp == kFwdMmaWarp) {
-    if (lane == 0) {
+    {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);  // S = Q K^T: N = 64
       constexpr uint32_t id_o = idesc_bf16(128, D, false, true);    // O += P V: N = D, B MN
       const uint32_t t_o = tmem + C::T_O, t_q = tmem + C::T_QA;
-      bool ok = wait_bar(q_tmem, 0, abort_flag, prm.status);
+      bool ok = warp_wait(q_tmem, 0, abort_flag, prm.status);
       // O += P(t) V(t), A = bf16 P from TMEM, contraction over the 64 keys
       auto issue_pv = [&](int t) -> bool {
         const int pb = t & 1, vs = t % C::VSTAGES;
-        if (!wait_bar(p_full + pb, (t >> 1) & 1, abort_flag, prm.status)) return false;
-        if (!wait_bar(v_full + vs, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
+        if (!warp_wait(p_full + pb, (t >> 1) & 1, abort_flag, prm.status)) return false;
+        if (!warp_wait(v_full + vs, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
         const uint32_t v_mn = opaque(lo_mnmajor(sb + C::OFF_V + vs * C::KB, C::BN * 128));
         const uint32_t t_p = tmem + C::T_P(pb);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts(t_o, t_p + 8 * k, v_mn + kstep_off(k), id_o, (t > 0 || k > 0) ? 1u : 0u);
-        mma_commit(p_empty + pb);
-        mma_commit(v_empty + vs);
+          mma_ts_w(t_o, t_p + 8 * k, v_mn + kstep_off(k), id_o, (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit_w(p_empty + pb);
+        mma_commit_w(v_empty + vs);
         return true;
       };
       for (int i = 0; ok && i < I; ++i) {
         const int s = i % C::KSTAGES, b = i & 1;
-        if (!wait_bar(k_full + s, (i / C::KSTAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
-        if (i >= 2 && !wait_bar(s_empty + b, ((i >> 1) - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (!warp_wait(k_full + s, (i / C::KSTAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (i >= 2 && !warp_wait(s_empty + b, ((i >> 1) - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_lo = opaque(lo_kmajor(sb + C::OFF_K + s * C::KB));
         const uint32_t t_s = tmem + C::T_S(b);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ts(t_s, t_q + 8 * k, k_lo + kslice_off(C::BN, k), id_s, k > 0 ? 1u : 0u);
-        mma_commit(s_full + b);
-        mma_commit(k_empty + s);
+          mma_ts_w(t_s, t_q + 8 * k, k_lo + kslice_off(C::BN, k), id_s, k > 0 ? 1u : 0u);
+        mma_commit_w(s_full + b);
+        mma_commit_w(k_empty + s);
         if (i >= T + 1 && !issue_pv(i - T - 1)) { ok = false; break; }
       }
-      if (ok && issue_pv(T - 1)) mma_commit(o_done);
+      if (ok && issue_pv(T - 1)) mma_commit_w(o_done);
       // every MMA this thread issued has completed before TMEM is released
-      mma_commit(drain);
+      mma_commit_w(drain);
       mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
     }
   } else {
@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else if (warp == kBwdMmaWarp) {
-    if (lane == 0) {
+    {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
       constexpr uint32_t id_sc = idesc_bf16(128, 64, false, false);  // scores: M=128 N=64
       constexpr uint32_t id_out = idesc_bf16(128, D, false, true);   // dK/dV: N=D, B MN
       constexpr uint32_t id_dq = idesc_bf16(D, 64, true, true);      // dQ^T: M=D, A,B MN
@@ -572,53 +572,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
         const uint32_t q_lo = opaque(lo_kmajor(sb + C::OFF_Q + s * C::QB));
         const uint32_t v_l = opaque(v_lo), k_l = opaque(k_lo);
-        if (!wait_bar(do_full + ds, (t / C::DSTAGES) & 1, abort_flag, prm.status)) return false;
+        if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
+          mma_ss_w(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
                  k > 0 ? 1u : 0u);
-        if (!wait_bar(q_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
+        if (!warp_wait(q_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(t_s, k_l + kslice_off(C::BM, k), q_lo + kslice_off(C::BN, k), id_sc,
+          mma_ss_w(t_s, k_l + kslice_off(C::BM, k), q_lo + kslice_off(C::BN, k), id_sc,
                  k > 0 ? 1u : 0u);
-        mma_commit(sc_full);
+        mma_commit_w(sc_full);
         return true;
       };
-      bool ok = wait_bar(kv_full, 0, abort_flag, prm.status) && issue_scores(0);
+      bool ok = warp_wait(kv_full, 0, abort_flag, prm.status) && issue_scores(0);
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES, ds = t % C::DSTAGES;
         const uint32_t q_mn = opaque(lo_mnmajor(sb + C::OFF_Q + s * C::QB, C::BN * 128));
         const uint32_t do_mn = opaque(lo_mnmajor(sb + C::OFF_DO + ds * C::QB, C::BN * 128));
         const uint32_t k_m = opaque(k_mn), ds_m = opaque(ds_mn);
         const uint32_t first = t > 0 ? 1u : 0u;
-        if (!wait_bar(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (!warp_wait(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
         // dK += dS^T Q first: it releases the Q stage
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts(t_dk, t_dp + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-        mma_commit(q_empty + s);
+          mma_ts_w(t_dk, t_dp + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+        mma_commit_w(q_empty + s);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts(t_dv, t_s + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-        mma_commit(do_empty + ds);
+          mma_ts_w(t_dv, t_s + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+        mma_commit_w(do_empty + ds);
         if (t >= 1) {
-          if (!wait_bar(dq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+          if (!warp_wait(dq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
           tc_fence_after();
         }
 #pragma unroll
         for (int k = 0; k < C::BM / 16; ++k)  // contraction over the 128 keys
-          mma_ss(t_dq, k_m + kstep_off(k), ds_m + kstep_off(k), id_dq, k > 0 ? 1u : 0u);
-        mma_commit(dq_full);
+          mma_ss_w(t_dq, k_m + kstep_off(k), ds_m + kstep_off(k), id_dq, k > 0 ? 1u : 0u);
+        mma_commit_w(dq_full);
         // the next tile's scores overwrite the A operands read above; MMAs
         // from one thread run in issue order
         if (t + 1 < T && !issue_scores(t + 1)) { ok = false; break; }
       }
-      if (ok) mma_commit(acc_done);
-      mma_commit(drain);
+      if (ok) mma_commit_w(acc_done);
+      mma_commit_w(drain);
       mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
     }
   } else {
