@@ -649,11 +649,12 @@ __global__ void __launch_bounds__(kColThreads, 1)
       if (!ok) break;
       // the stage's scalars were last read by the elementwise warps of tile
       // t - STAGES, which finished before the gradK MMAs that freed the stage
+      // stored negated: every one of them is subtracted
       float* sc = scal + s * 4 * C::BN;
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = pre[a][u];
+        for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = -pre[a][u];
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(qg_full + s, (has_gq ? 2 : 1) * C::QB);
@@ -786,6 +787,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
     const int j = j0 + row;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sc2 = prm.scale * kLog2e;
+    const f2 sc2_2 = {sc2, sc2}, scale_2 = {prm.scale, prm.scale};
     const bool has_g = has_gq || has_gk, has_h = has_gv;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
@@ -807,33 +809,35 @@ __global__ void __launch_bounds__(kColThreads, 1)
       auto body = [&](auto masked) {
 #pragma unroll
         for (int c4 = 0; c4 < NC / 4; ++c4) {  // 4 query columns per step
+          // negated row scalars of the 4 queries: -LSE log2 e, -D, -r, -sigma
           const float4 L = sc4[c4], Dd = sc4[C::BN / 4 + c4], R = sc4[C::BN / 2 + c4],
                        Sg = sc4[3 * C::BN / 4 + c4];
-          const float lv[4] = {L.x, L.y, L.z, L.w}, dv[4] = {Dd.x, Dd.y, Dd.z, Dd.w},
-                      rv[4] = {R.x, R.y, R.z, R.w}, sv[4] = {Sg.x, Sg.y, Sg.z, Sg.w};
-          float o_ds[4], o_gd[4], o_gs[4];
+          const f2 nl[2] = {{L.x, L.y}, {L.z, L.w}}, nd[2] = {{Dd.x, Dd.y}, {Dd.z, Dd.w}},
+                   nr[2] = {{R.x, R.y}, {R.z, R.w}}, ns[2] = {{Sg.x, Sg.y}, {Sg.z, Sg.w}};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int cc = 4 * c4 + e;
-            float p = ex2_approx(__uint_as_float(sr[cc]) * sc2 - lv[e]);
+          for (int hh = 0; hh < 2; ++hh) {  // query columns cc, cc + 1: one packed pair
+            const int cc = 4 * c4 + 2 * hh;
+            const f2 sv2 = {__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])};
+            const f2 x = fma2(sv2, sc2_2, nl[hh]);
+            f2 p = {ex2_approx(x.x), ex2_approx(x.y)};
             if (decltype(masked)::value) {
               const int q = qa + cc;
-              p = (q < N && j < N && (!prm.causal || q >= j)) ? p : 0.f;
+              p.x = (q < N && j < N && (!prm.causal || q >= j)) ? p.x : 0.f;
+              p.y = (q + 1 < N && j < N && (!prm.causal || q + 1 >= j)) ? p.y : 0.f;
             }
-            const float dpm = __uint_as_float(dpr[cc]) - dv[e];
+            const f2 dpm = add2({__uint_as_float(dpr[cc]), __uint_as_float(dpr[cc + 1])}, nd[hh]);
             // G^T (H^T) is zero, its TMEM columns unwritten, without gQ and gK (gV)
-            const float gm = has_g ? fmaf(__uint_as_float(gr[cc]), prm.scale, -rv[e]) : -rv[e];
-            const float hv = has_h ? __uint_as_float(hr[cc]) : 0.f;
-            o_ds[e] = p * dpm;
-            o_gd[e] = p * gm;
-            o_gs[e] = p * (fmaf(gm, dpm, hv) - sv[e]);
+            const f2 gm = has_g ? fma2({__uint_as_float(gr[cc]), __uint_as_float(gr[cc + 1])},
+                                       scale_2, nr[hh])
+                                : nr[hh];
+            const f2 hv = has_h ? f2{__uint_as_float(hr[cc]), __uint_as_float(hr[cc + 1])}
+                                : f2{0.f, 0.f};
+            const f2 ds = mul2(p, dpm), gd = mul2(p, gm);
+            const f2 gs = mul2(p, add2(fma2(gm, dpm, hv), ns[hh]));
+            dsw[cc >> 1] = pack_bf16(ds.x, ds.y);
+            gdw[cc >> 1] = pack_bf16(gd.x, gd.y);
+            gsw[cc >> 1] = pack_bf16(gs.x, gs.y);
           }
-          dsw[2 * c4] = pack_bf16(o_ds[0], o_ds[1]);
-          dsw[2 * c4 + 1] = pack_bf16(o_ds[2], o_ds[3]);
-          gdw[2 * c4] = pack_bf16(o_gd[0], o_gd[1]);
-          gdw[2 * c4 + 1] = pack_bf16(o_gd[2], o_gd[3]);
-          gsw[2 * c4] = pack_bf16(o_gs[0], o_gs[1]);
-          gsw[2 * c4 + 1] = pack_bf16(o_gs[2], o_gs[3]);
         }
       };
       if (need_mask)
