@@ -336,9 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t srow = (size_t)bh * N + (row_ok ? i : 0);
     const float lse2 = row_ok ? prm.lse[srow] * kLog2e : 0.f;
     const float sc2 = prm.scale * kLog2e;
+    const f2 sc2_2 = {sc2, sc2}, nlse2 = {-lse2, -lse2}, scale_2 = {prm.scale, prm.scale};
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const bool has_g = has_gq || has_gk;
-    float r_acc = 0.f;
+    f2 r_acc = {0.f, 0.f};  // even and odd keys summed apart
     bool ok = warp_wait(q_full, 0, abort_flag, prm.status);
     if (ok) {
       // stationary Q and gQ rows -> TMEM (bf16 pairs, lower half = even
@@ -381,20 +382,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pw[16], pgw[16];
       auto body = [&](auto masked) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float p0 = ex2_approx(__uint_as_float(sr[c]) * sc2 - lse2);
-          float p1 = ex2_approx(__uint_as_float(sr[c + 1]) * sc2 - lse2);
+        for (int c = 0; c < 32; c += 2) {  // keys c, c + 1: one packed pair
+          const f2 x = fma2({__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, sc2_2, nlse2);
+          f2 p = {ex2_approx(x.x), ex2_approx(x.y)};
           if (decltype(masked)::value) {
             const int jj = j0 + c;
-            p0 = (row_ok && jj < N && (!prm.causal || jj <= i)) ? p0 : 0.f;
-            p1 = (row_ok && jj + 1 < N && (!prm.causal || jj + 1 <= i)) ? p1 : 0.f;
+            p.x = (row_ok && jj < N && (!prm.causal || jj <= i)) ? p.x : 0.f;
+            p.y = (row_ok && jj + 1 < N && (!prm.causal || jj + 1 <= i)) ? p.y : 0.f;
           }
           // G is zero (and its TMEM columns unwritten) without gQ and gK
-          const float g0 = has_g ? p0 * (__uint_as_float(gr[c]) * prm.scale) : 0.f;
-          const float g1 = has_g ? p1 * (__uint_as_float(gr[c + 1]) * prm.scale) : 0.f;
-          r_acc += g0 + g1;
-          pw[c >> 1] = pack_bf16(p0, p1);
-          pgw[c >> 1] = pack_bf16(g0, g1);
+          const f2 pg = has_g ? mul2(p, mul2({__uint_as_float(gr[c]), __uint_as_float(gr[c + 1])},
+                                             scale_2))
+                              : f2{0.f, 0.f};
+          r_acc = add2(r_acc, pg);
+          pw[c >> 1] = pack_bf16(p.x, p.y);
+          pgw[c >> 1] = pack_bf16(pg.x, pg.y);
         }
       };
       if (need_mask)
@@ -412,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     if (ok) ok = warp_wait(w_done, 0, abort_flag, prm.status);
     tc_fence_after();
-    part[half * 128 + row] = r_acc;
+    part[half * 128 + row] = r_acc.x + r_acc.y;
     consumer_sync();
     const float r = part[row] + part[128 + row];
     float dd = 0.f, sg = 0.f;
@@ -488,17 +490,27 @@ struct Col {
   static constexpr uint32_t OFF_QG = 4 * KB;                     // [STAGES][2 * QB]
   static constexpr uint32_t OFF_DO = OFF_QG + STAGES * 2 * QB;   // [DSTAGES][QB]
   static constexpr uint32_t OFF_DS = OFF_DO + DSTAGES * QB, OFF_GS = OFF_DS + XB;
-  static constexpr uint32_t OFF_SC = OFF_GS + XB;          // [STAGES][4][BN] fp32
-  static constexpr uint32_t OFF_MISC = OFF_SC + STAGES * 4 * BN * 4;
+  // row scalars: one buffer more than [Q|gQ] stages, so the producer can
+  // write a tile's scalars before its stage is free
+  static constexpr int SCSTAGES = STAGES + 1;
+  static constexpr uint32_t OFF_SC = OFF_GS + XB;          // [SCSTAGES][4][BN] fp32
+  static constexpr uint32_t OFF_MISC = OFF_SC + SCSTAGES * 4 * BN * 4;
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "pass 2 shared memory budget");
   // TMEM columns
-  // S^T and G^T adjacent: one N=128 MMA chain writes [S^T | K gQ^T].  After
-  // the elementwise warps have read a tile's scores they overwrite, inside
-  // the 16 columns each of them read, G^T with bf16 gS^T, dP^T with bf16
-  // dS^T and H^T with bf16 gdP^T: the A operands of the gradK / gradV MMAs.
+  // S^T and G^T adjacent: one N=128 MMA chain writes [S^T | K gQ^T].  Once
+  // the elementwise warps have read a tile's four score blocks, the next
+  // tile's dP^T and H^T are computed into their columns while the
+  // elementwise phase runs.  The bf16 A operands of the gradK / gradV MMAs go
+  // inside the 16 columns each thread read: gS^T into the first 8 and dS^T
+  // into the last 8 of S^T, gdP^T into the first 8 of G^T.
   static constexpr uint32_t T_S = 0, T_G = 64, T_DP = 128, T_H = 192, T_GK = 256, T_GV = 256 + D;
+  // At d = 128 the next tile's dP^T, H^T are issued as soon as the scores
+  // have been read, so that they run during the elementwise phase.  At d = 64
+  // ([Q|gQ] double-buffered) issuing them after the gradient MMAs measured
+  // faster.
+  static constexpr bool EARLY_DH = D == 128;
   // gradQ^T partial (64 columns): its own region when TMEM has room (d = 64),
   // else the S^T columns, which the next tile rewrites last (d = 128)
   static constexpr bool GQ_IN_S = (256 + 2 * D + 64 > 512);
@@ -556,11 +568,14 @@ __global__ void __launch_bounds__(kColThreads, 1)
   uint64_t* do_full = qg_empty + C::STAGES;     // [DSTAGES]
   uint64_t* do_empty = do_full + C::DSTAGES;    // [DSTAGES]: gradV MMAs done with dO
   uint64_t* sc_full = do_empty + C::DSTAGES;    // scores in TMEM
-  uint64_t* ds_full = sc_full + 1;              // A operands in TMEM, dS^T / gS^T in smem
+  uint64_t* sc_read = sc_full + 1;              // elementwise warps hold the scores
+  uint64_t* ds_full = sc_read + 1;              // A operands in TMEM, dS^T / gS^T in smem
   uint64_t* gq_full = ds_full + 1;
   uint64_t* gq_empty = gq_full + 1;
   uint64_t* acc_done = gq_empty + 1;
   uint64_t* drain = acc_done + 1;
+  static_assert((8 + 2 * C::STAGES + 2 * C::DSTAGES) * 8 <= 256,
+                "barriers end below the TMEM slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
   float* scal = reinterpret_cast<float*>(smem + C::OFF_SC);
@@ -584,6 +599,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
       mbar_init(do_empty + s, 1);
     }
     mbar_init(sc_full, 1);
+    mbar_init(sc_read, kColConsumers);
     mbar_init(ds_full, kColConsumers);
     mbar_init(gq_full, 1);
     mbar_init(gq_empty, kColConsumers);
@@ -632,6 +648,16 @@ __global__ void __launch_bounds__(kColThreads, 1)
       const int s = t % C::STAGES, ds = t % C::DSTAGES;
       const int q0 = qstart + rotated(t, rot, T) * C::BN;
       const int q_next = qstart + rotated(t + 1 < T ? t + 1 : 0, rot, T) * C::BN;
+      // Row scalars of tile t, stored negated (every one of them is
+      // subtracted).  Their buffer was last read by the elementwise warps of
+      // tile t - SCSTAGES, which finished before that tile's gradK MMAs
+      // released its [Q|gQ] stage, awaited in the previous iteration.
+      float* sc = scal + (t % C::SCSTAGES) * 4 * C::BN;
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = -pre[a][u];
+      __syncwarp();
       // dO first: its ring is deeper, so it runs ahead of [Q|gQ]
       bool w = true;
       if (lane == 0) {
@@ -647,16 +673,8 @@ __global__ void __launch_bounds__(kColThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       if (!ok) break;
-      // the stage's scalars were last read by the elementwise warps of tile
-      // t - STAGES, which finished before the gradK MMAs that freed the stage
-      // stored negated: every one of them is subtracted
-      float* sc = scal + s * 4 * C::BN;
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = -pre[a][u];
-      __syncwarp();
       if (lane == 0) {
+        // this arrival publishes the scalars written above with the stage
         mbar_arrive_expect_tx(qg_full + s, (has_gq ? 2 : 1) * C::QB);
         load_pair_opt<D>(smem + C::OFF_QG + s * 2 * C::QB, &mQ, &mGQ, has_gq, qg_full + s,
                          C::BN, q0, bh);
@@ -696,13 +714,12 @@ __global__ void __launch_bounds__(kColThreads, 1)
       const uint32_t t_s = tmem + C::T_S, t_g = tmem + C::T_G, t_dp = tmem + C::T_DP,
                      t_h = tmem + C::T_H, t_gk = tmem + C::T_GK, t_gv = tmem + C::T_GV,
                      t_gq = tmem + C::T_GQ;
-      // scores of tile t: dP^T and H^T (need dO) first, then S^T, G^T (need Q, gQ)
-      auto issue_scores = [&](int t) -> bool {
-        const int s = t % C::STAGES, ds = t % C::DSTAGES;
+      // dP^T and H^T of tile t (need dO(t) and the previous tile's scores
+      // read out of TMEM)
+      auto issue_dh = [&](int t) -> bool {
+        const int ds = t % C::DSTAGES;
         const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
-        const uint32_t qgq_lo = opaque(lo_kmajor(sb + C::OFF_QG + s * 2 * C::QB));  // [Q;gQ] per half
-        const uint32_t v_l = opaque(v_lo), gv_l = opaque(gv_lo), k_l = opaque(k_lo),
-                       gk_l = opaque(gk_lo);
+        const uint32_t v_l = opaque(v_lo), gv_l = opaque(gv_lo);
         if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
@@ -714,6 +731,15 @@ __global__ void __launch_bounds__(kColThreads, 1)
             mma_ss_w(t_h, gv_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
                    k > 0 ? 1u : 0u);
         }
+        return true;
+      };
+      // S^T and G^T of tile t (need Q, gQ; overwrite the A operands of tile
+      // t - 1 and, at d = 128, its gradQ^T partial), then the commit that
+      // covers all four score blocks
+      auto issue_sg = [&](int t) -> bool {
+        const int s = t % C::STAGES;
+        const uint32_t qgq_lo = opaque(lo_kmajor(sb + C::OFF_QG + s * 2 * C::QB));  // [Q;gQ] per half
+        const uint32_t k_l = opaque(k_lo), gk_l = opaque(gk_lo);
         if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
         if (C::GQ_IN_S && t >= 1 && !warp_wait(gq_empty, (t - 1) & 1, abort_flag, prm.status))
           return false;
@@ -735,9 +761,18 @@ __global__ void __launch_bounds__(kColThreads, 1)
         mma_commit_w(sc_full);
         return true;
       };
-      bool ok = warp_wait(kv_full, 0, abort_flag, prm.status) && issue_scores(0);
+      bool ok = warp_wait(kv_full, 0, abort_flag, prm.status) && issue_dh(0) && issue_sg(0);
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES, ds = t % C::DSTAGES;
+        // ---- next tile's dP^T, H^T while the elementwise warps work ----
+        if (C::EARLY_DH && t + 1 < T) {
+          if (!warp_wait(sc_read, t & 1, abort_flag, prm.status)) { ok = false; break; }
+          tc_fence_after();
+          if (!issue_dh(t + 1)) { ok = false; break; }
+        }
+        // ---- outputs: A operands (bf16 gS^T, dS^T, gdP^T) from TMEM ----
+        if (!warp_wait(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+        tc_fence_after();
         const uint32_t qgq_s = sb + C::OFF_QG + s * 2 * C::QB;
         // B operands MN-major: 64-feature groups 2*BN*128 bytes apart in the
         // interleaved [Q;gQ] stage, BN*128 apart in the dO tile
@@ -747,33 +782,32 @@ __global__ void __launch_bounds__(kColThreads, 1)
         const uint32_t k_m = opaque(k_mn), gk_m = opaque(gk_mn), ds_m = opaque(ds_mn),
                        gs_m = opaque(gs_mn);
         const uint32_t first = t > 0 ? 1u : 0u;
-        // ---- outputs: A operands (bf16 gS^T, dS^T, gdP^T) from TMEM ----
-        if (!warp_wait(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
-        tc_fence_after();
         // gradK first: it releases the [Q|gQ] stage that the next tile waits for
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 queries
-          mma_ts_w(t_gk, t_g + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-          if (has_gq) mma_ts_w(t_gk, t_dp + 16 * k, gq_mn + kstep_off(k), id_out, 1u);
+          mma_ts_w(t_gk, t_s + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+          if (has_gq) mma_ts_w(t_gk, t_s + 16 * k + 8, gq_mn + kstep_off(k), id_out, 1u);
         }
         mma_commit_w(qg_empty + s);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts_w(t_gv, t_h + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+          mma_ts_w(t_gv, t_g + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
         mma_commit_w(do_empty + ds);
         if (!C::GQ_IN_S && t >= 1) {
           if (!warp_wait(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
           tc_fence_after();
         }
+        // at d = 128 this overwrites S^T, whose A operands the gradK MMAs
+        // above read first: MMAs from one thread run in issue order
 #pragma unroll
         for (int k = 0; k < C::BM / 16; ++k) {  // contraction over the 128 keys
           mma_ss_w(t_gq, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
           if (has_gk) mma_ss_w(t_gq, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
         }
         mma_commit_w(gq_full);
-        // the next tile's scores overwrite the A operands read above; MMAs
-        // from one thread run in issue order
-        if (t + 1 < T && !issue_scores(t + 1)) { ok = false; break; }
+        // without EARLY_DH, ds_full (all scores read) has already freed dP^T, H^T
+        if (!C::EARLY_DH && t + 1 < T && !issue_dh(t + 1)) { ok = false; break; }
+        if (t + 1 < T && !issue_sg(t + 1)) { ok = false; break; }
       }
       if (ok) mma_commit_w(acc_done);
       mma_commit_w(drain);
@@ -800,7 +834,12 @@ __global__ void __launch_bounds__(kColThreads, 1)
       uint32_t sr[NC], dpr[NC], gr[NC], hr[NC];
       const uint32_t tl = tmem + lane_off + NC * slice;
       tmem_ld16x4(tl + C::T_S, tl + C::T_DP, tl + C::T_G, tl + C::T_H, sr, dpr, gr, hr);
-      const float4* sc4 = reinterpret_cast<const float4*>(scal + s * 4 * C::BN + NC * slice);
+      if (C::EARLY_DH) {  // the loads above have completed: dP^T, H^T are free
+        tc_fence_before();
+        mbar_arrive(sc_read);
+      }
+      const float4* sc4 =
+          reinterpret_cast<const float4*>(scal + (t % C::SCSTAGES) * 4 * C::BN + NC * slice);
       const int qa = q0 + NC * slice;
       const bool need_mask = (qa + NC > N) || (j0 + C::BM > N) || (prm.causal && qa < j0 + C::BM);
       uint32_t dsw[NC / 2], gdw[NC / 2], gsw[NC / 2];
@@ -845,9 +884,10 @@ __global__ void __launch_bounds__(kColThreads, 1)
       else
         body(std::false_type{});
       // A operands of the gradK / gradV MMAs: bf16 pairs (low half = even
-      // query) in the first 8 of the 16 columns this thread read from G^T,
-      // dP^T and H^T; one 16-query contraction step per slice
-      tmem_st8x3(tl + C::T_G, gsw, tl + C::T_DP, dsw, tl + C::T_H, gdw);
+      // query), gS^T and dS^T in the 16 columns this thread read from S^T,
+      // gdP^T in the first 8 it read from G^T; one 16-query contraction step
+      // per slice
+      tmem_st8x3(tl + C::T_S, gsw, tl + C::T_S + 8, dsw, tl + C::T_G, gdw);
       // dS^T and gS^T also go to shared memory as the gradQ^T B operands; the
       // buffers of tile t-1 were released by gq_full(t-1), awaited below.
       // This thread's columns are 16-byte chunks [NC*slice/8, +NC/8) of its row.
