@@ -6,11 +6,12 @@
 //   dP = dO V^T,  D_i = dO_i . O_i,  dS = P*(dP - D),
 //   dQ = c dS K,  dK = c dS^T Q,  dV = P^T dO.
 //
-// forward (row-stationary, 128 query rows per CTA, 64-key tiles): two sweeps
-//   over the key tiles.  The first reduces each row's log-sum-exp from S in
-//   TMEM (running max and sum in registers); the second forms the exactly
-//   normalised P = exp(S - LSE) in bf16 into TMEM and accumulates O += P V
-//   there.  O never needs rescaling, at the price of S computed twice.
+// forward (row-stationary, 128 query rows per CTA, 128-key tiles): two
+//   sweeps over the key tiles.  The first reduces each row's log-sum-exp from
+//   S in TMEM (running max and sum in registers); the second forms the exactly
+//   normalised P = exp(S - LSE) in bf16, in place of S in TMEM, and
+//   accumulates O += P V there.  O never needs rescaling, at the price of S
+//   computed twice.
 // first backward (key-stationary, 128 key rows per CTA, 64-query tiles):
 //   S^T and dP^T into TMEM; bf16 P^T and dS^T written back into TMEM as the
 //   A operands of dV += P^T dO and dK += dS^T Q; dQ^T partial = K^T dS^T
@@ -39,7 +40,7 @@ using namespace tc;
 namespace {
 
 // Forward warp roles: warps 0-15 elementwise (warp w: TMEM lane quadrant
-// w % 4, 16-key slice w / 4 of the 64-key tile), warp 16 TMA producer,
+// w % 4, 32-key slice w / 4 of the 128-key tile), warp 16 TMA producer,
 // warp 17 TMEM allocator and MMA issuer.
 constexpr int kFwdConsumerWarps = 16;
 constexpr int kFwdConsumers = kFwdConsumerWarps * 32;
@@ -47,7 +48,7 @@ constexpr int kFwdProducerWarp = kFwdConsumerWarps;
 constexpr int kFwdMmaWarp = kFwdConsumerWarps + 1;
 constexpr int kFwdThreads = (kFwdConsumerWarps + 2) * 32;
 constexpr int kFwdSlices = kFwdConsumerWarps / 4;  // column slices per row
-constexpr int kFwdCols = 64 / kFwdSlices;           // key columns per thread
+constexpr int kFwdCols = 128 / kFwdSlices;          // key columns per thread
 constexpr float kLn2 = 0.6931471805599453f;
 
 // ===========================================================================
@@ -55,8 +56,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 // ===========================================================================
 template <int D>
 struct Fwd {
-  static constexpr int BM = 128, BN = 64;
-  static constexpr int KSTAGES = 4, VSTAGES = 3;
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int KSTAGES = D == 128 ? 3 : 4, VSTAGES = D == 128 ? 2 : 3;
   static constexpr uint32_t QB = BM * D * 2;   // stationary Q tile
   static constexpr uint32_t KB = BN * D * 2;   // one streamed K or V tile
   static constexpr uint32_t OFF_Q = 0, OFF_K = QB, OFF_V = OFF_K + KSTAGES * KB;
@@ -65,12 +66,14 @@ struct Fwd {
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "forward shared memory budget");
-  // TMEM columns: S (two buffers), O, bf16 P (two buffers), bf16 Q as the A
-  // operand of S = Q K^T
-  static constexpr uint32_t T_O = 128, TMEM_COLS = 512;
-  __host__ __device__ static constexpr uint32_t T_S(int b) { return 64u * b; }
-  __host__ __device__ static constexpr uint32_t T_P(int b) { return 128u + D + 32u * b; }
-  static constexpr uint32_t T_QA = 128 + D + 64;
+  // TMEM columns: S (two buffers of 128), O, bf16 Q as the A operand of
+  // S = Q K^T.  In the second sweep each elementwise thread writes bf16 P
+  // into the first 16 of the 32 S columns it read: keys 32s + 2c, + 1 of
+  // slice s in column 32s + c, so 16-key step k of P V sits at p_col(k).
+  static constexpr uint32_t T_O = 256, TMEM_COLS = 512;
+  __host__ __device__ static constexpr uint32_t T_S(int b) { return 128u * b; }
+  __host__ __device__ static constexpr uint32_t p_col(int k) { return 32u * (k >> 1) + 8u * (k & 1); }
+  static constexpr uint32_t T_QA = 256 + D;
   static_assert(T_QA + D / 2 <= TMEM_COLS, "forward TMEM budget");
 };
 
@@ -100,10 +103,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint64_t* v_full = k_empty + C::KSTAGES;       // [VSTAGES]
   uint64_t* v_empty = v_full + C::VSTAGES;       // [VSTAGES]
   uint64_t* s_full = v_empty + C::VSTAGES;       // [2]
-  uint64_t* s_empty = s_full + 2;                // [2]
-  uint64_t* p_full = s_empty + 2;                // [2]
-  uint64_t* p_empty = p_full + 2;                // [2]
-  uint64_t* o_done = p_empty + 2;
+  uint64_t* s_empty = s_full + 2;                // [2]: S read out of TMEM
+  uint64_t* p_full = s_empty + 2;                // [2]: bf16 P written over S
+  uint64_t* o_done = p_full + 2;
   uint64_t* q_tmem = o_done + 1;
   uint64_t* drain = q_tmem + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
@@ -136,7 +138,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(s_full + b, 1);
       mbar_init(s_empty + b, kFwdConsumers);
       mbar_init(p_full + b, kFwdConsumers);
-      mbar_init(p_empty + b, 1);
     }
     mbar_init(o_done, 1);
     mbar_init(q_tmem, kFwdConsumers);
@@ -190,25 +191,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == kFwdMmaWarp) {
     {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
-      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);  // S = Q K^T: N = 64
+      constexpr uint32_t id_s = idesc_bf16(128, C::BN, false, false);  // S = Q K^T: N = BN
       constexpr uint32_t id_o = idesc_bf16(128, D, false, true);    // O += P V: N = D, B MN
       const uint32_t t_o = tmem + C::T_O, t_q = tmem + C::T_QA;
       bool ok = warp_wait(q_tmem, 0, abort_flag, prm.status);
-      // O += P(t) V(t), A = bf16 P from TMEM, contraction over the 64 keys
+      // O += P(t) V(t), A = bf16 P from TMEM (in the S buffer of iteration
+      // T + t), contraction over the tile's keys
       auto issue_pv = [&](int t) -> bool {
         const int pb = t & 1, vs = t % C::VSTAGES;
         if (!warp_wait(p_full + pb, (t >> 1) & 1, abort_flag, prm.status)) return false;
         if (!warp_wait(v_full + vs, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
         const uint32_t v_mn = opaque(lo_mnmajor(sb + C::OFF_V + vs * C::KB, C::BN * 128));
-        const uint32_t t_p = tmem + C::T_P(pb);
+        const uint32_t t_p = tmem + C::T_S((T + t) & 1);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts_w(t_o, t_p + 8 * k, v_mn + kstep_off(k), id_o, (t > 0 || k > 0) ? 1u : 0u);
-        mma_commit_w(p_empty + pb);
+          mma_ts_w(t_o, t_p + C::p_col(k), v_mn + kstep_off(k), id_o, (t > 0 || k > 0) ? 1u : 0u);
         mma_commit_w(v_empty + vs);
         return true;
       };
+      // S(i) reuses the buffer of iteration i - 2: read out (s_empty) and, in
+      // the second sweep, its P consumed by the P V MMAs of iteration i - 1,
+      // which run before S(i) in issue order
       for (int i = 0; ok && i < I; ++i) {
         const int s = i % C::KSTAGES, b = i & 1;
         if (!warp_wait(k_full + s, (i / C::KSTAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
@@ -237,6 +241,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const bool row_ok = i < N;
     const size_t srow = (size_t)bh * N + (row_ok ? i : 0);
     const float sc2 = prm.scale * kLog2e;
+    const f2 sc2_2 = {sc2, sc2};
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     bool ok = warp_wait(q_full, 0, abort_flag, prm.status);
     if (ok) {
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int b = it & 1;
       if (!warp_wait(s_full + b, (it >> 1) & 1, abort_flag, prm.status)) return false;
       tc_fence_after();
-      tmem_ld16(tmem + lane_off + C::T_S(b) + NC * slice, sr);
+      tmem_ld32(tmem + lane_off + C::T_S(b) + NC * slice, sr);
       tc_fence_before();
       mbar_arrive(s_empty + b);
       return true;
@@ -276,27 +281,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!load_s(t, sr)) { ok = false; break; }
       const int j0 = rotated(t, rot, T) * C::BN + NC * slice;
       const bool need_mask = !row_ok || (j0 + NC > N) || (prm.causal && j0 + NC - 1 > i);
+      // raw maximum first (c log2 e > 0 preserves the order); masked
+      // entries become -inf, which the sum below turns into 2^-inf = 0
       float mx = -INFINITY;
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const int j = j0 + c;
-        const bool in = !need_mask || (row_ok && j < N && (!prm.causal || j <= i));
-        mx = in ? fmaxf(mx, __uint_as_float(sr[c]) * sc2) : mx;
+        for (int c = 0; c < NC; ++c) {
+          const int j = j0 + c;
+          const bool in = row_ok && j < N && (!prm.causal || j <= i);
+          const float v = in ? __uint_as_float(sr[c]) : -INFINITY;
+          sr[c] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
       }
+      mx *= sc2;
       if (mx > m2) {
         l *= ex2_approx(m2 - mx);  // 2^(-inf) = 0 on the first update
         m2 = mx;
       }
       if (m2 > -INFINITY) {
-        float acc = 0.f;
+        const f2 nm = {-m2, -m2};
+        f2 acc = {0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          const int j = j0 + c;
-          const bool in = !need_mask || (row_ok && j < N && (!prm.causal || j <= i));
-          const float e = ex2_approx(__uint_as_float(sr[c]) * sc2 - m2);
-          acc += in ? e : 0.f;
+        for (int c = 0; c < NC; c += 2) {
+          const f2 x = fma2({__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, sc2_2, nm);
+          acc = add2(acc, f2{ex2_approx(x.x), ex2_approx(x.y)});
         }
-        l += acc;
+        l += acc.x + acc.y;
       }
     }
     // combine the column slices of each row (every consumer thread gets here,
@@ -324,10 +338,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool need_mask = !row_ok || (j0 + NC > N) || (prm.causal && j0 + NC - 1 > i);
       uint32_t pw[NC / 2];
       auto body = [&](auto masked) {
+        const f2 nl = {-lse2, -lse2};
 #pragma unroll
         for (int c = 0; c < NC; c += 2) {
-          float p0 = ex2_approx(__uint_as_float(sr[c]) * sc2 - lse2);
-          float p1 = ex2_approx(__uint_as_float(sr[c + 1]) * sc2 - lse2);
+          const f2 x = fma2({__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, sc2_2, nl);
+          float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
           if (decltype(masked)::value) {
             const int j = j0 + c;
             p0 = (row_ok && j < N && (!prm.causal || j <= i)) ? p0 : 0.f;
@@ -340,17 +355,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         body(std::true_type{});
       else
         body(std::false_type{});
-      const int pb = t & 1;
-      // P buffer pb was last read by the O MMAs of tile t-2
-      if (t >= 2 && !warp_wait(p_empty + pb, ((t >> 1) - 1) & 1, abort_flag, prm.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // keys NC*slice + 2c, + 1 in column NC/2*slice + c: one 16-key MMA step
-      tmem_st8(tmem + lane_off + C::T_P(pb) + (NC / 2) * slice, pw);
+      // bf16 P over the first 16 of the 32 S columns this thread read: keys
+      // NC*slice + 2c, + 1 in column NC*slice + c (two 16-key MMA steps)
+      tmem_st16(tmem + lane_off + C::T_S((T + t) & 1) + NC * slice, pw);
       tc_fence_before();
-      mbar_arrive(p_full + pb);
+      mbar_arrive(p_full + (t & 1));
     }
     // ---- epilogue: O (bf16) and LSE (natural log) ----
     ok = __all_sync(0xffffffffu, ok);
