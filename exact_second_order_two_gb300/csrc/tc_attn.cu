@@ -412,9 +412,12 @@ struct Bwd {
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "backward shared memory budget");
   // TMEM columns.  After the elementwise warps have read a tile's scores they
-  // overwrite, inside the 16 columns each of them read, S^T with bf16 P^T and
-  // dP^T with bf16 dS^T: the A operands of the dV / dK MMAs.
+  // write, inside the 16 S^T columns each of them read, bf16 P^T (first 8)
+  // and dS^T (last 8): the A operands of the dV / dK MMAs.  The dP^T columns
+  // are then free for the next tile's dP^T, issued while the elementwise
+  // phase runs.
   static constexpr uint32_t T_S = 0, T_DP = 64, T_DK = 128, T_DV = 128 + D, T_DQ = 128 + 2 * D;
+  static constexpr bool EARLY_DP = true;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(T_DQ + 64 <= TMEM_COLS, "backward TMEM budget");
 };
@@ -456,7 +459,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* do_full = q_empty + C::STAGES;      // [DSTAGES]
   uint64_t* do_empty = do_full + C::DSTAGES;    // [DSTAGES]: dV MMAs done with dO
   uint64_t* sc_full = do_empty + C::DSTAGES;
-  uint64_t* ds_full = sc_full + 1;
+  uint64_t* sc_read = sc_full + 1;              // elementwise warps hold the scores
+  uint64_t* ds_full = sc_read + 1;
   uint64_t* dq_full = ds_full + 1;
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* acc_done = dq_empty + 1;
@@ -484,6 +488,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(do_empty + s, 1);
     }
     mbar_init(sc_full, 1);
+    mbar_init(sc_read, kBwdConsumers);
     mbar_init(ds_full, kBwdConsumers);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, kBwdConsumers);
@@ -575,18 +580,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t ds_mn = lo_mnmajor(sb + C::OFF_DS, 1024);
       const uint32_t t_s = tmem + C::T_S, t_dp = tmem + C::T_DP, t_dk = tmem + C::T_DK,
                      t_dv = tmem + C::T_DV, t_dq = tmem + C::T_DQ;
-      // scores of tile t: dP^T (needs dO) first, then S^T (needs Q)
-      auto issue_scores = [&](int t) -> bool {
-        const int s = t % C::STAGES, ds = t % C::DSTAGES;
+      // dP^T of tile t (needs dO(t) and the previous tile's dP^T read out)
+      auto issue_dp = [&](int t) -> bool {
+        const int ds = t % C::DSTAGES;
         const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
-        const uint32_t q_lo = opaque(lo_kmajor(sb + C::OFF_Q + s * C::QB));
-        const uint32_t v_l = opaque(v_lo), k_l = opaque(k_lo);
+        const uint32_t v_l = opaque(v_lo);
         if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_ss_w(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
                  k > 0 ? 1u : 0u);
+        return true;
+      };
+      // S^T of tile t (needs Q(t); overwrites the A operands of tile t - 1),
+      // then the commit that covers both score blocks
+      auto issue_s = [&](int t) -> bool {
+        const int s = t % C::STAGES;
+        const uint32_t q_lo = opaque(lo_kmajor(sb + C::OFF_Q + s * C::QB));
+        const uint32_t k_l = opaque(k_lo);
         if (!warp_wait(q_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
@@ -596,35 +608,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit_w(sc_full);
         return true;
       };
-      bool ok = warp_wait(kv_full, 0, abort_flag, prm.status) && issue_scores(0);
+      bool ok = warp_wait(kv_full, 0, abort_flag, prm.status) && issue_dp(0) && issue_s(0);
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES, ds = t % C::DSTAGES;
-        const uint32_t q_mn = opaque(lo_mnmajor(sb + C::OFF_Q + s * C::QB, C::BN * 128));
-        const uint32_t do_mn = opaque(lo_mnmajor(sb + C::OFF_DO + ds * C::QB, C::BN * 128));
-        const uint32_t k_m = opaque(k_mn), ds_m = opaque(ds_mn);
-        const uint32_t first = t > 0 ? 1u : 0u;
+        if (C::EARLY_DP && t + 1 < T) {
+          if (!warp_wait(sc_read, t & 1, abort_flag, prm.status)) { ok = false; break; }
+          tc_fence_after();
+          if (!issue_dp(t + 1)) { ok = false; break; }
+        }
         if (!warp_wait(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
-        // dK += dS^T Q first: it releases the Q stage
+        {
+          const uint32_t q_mn = opaque(lo_mnmajor(sb + C::OFF_Q + s * C::QB, C::BN * 128));
+          const uint32_t do_mn = opaque(lo_mnmajor(sb + C::OFF_DO + ds * C::QB, C::BN * 128));
+          const uint32_t first = t > 0 ? 1u : 0u;
+          // dK += dS^T Q first: it releases the Q stage
 #pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts_w(t_dk, t_dp + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-        mma_commit_w(q_empty + s);
+          for (int k = 0; k < C::BN / 16; ++k)
+            mma_ts_w(t_dk, t_s + 16 * k + 8, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+          mma_commit_w(q_empty + s);
 #pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts_w(t_dv, t_s + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-        mma_commit_w(do_empty + ds);
+          for (int k = 0; k < C::BN / 16; ++k)
+            mma_ts_w(t_dv, t_s + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+          mma_commit_w(do_empty + ds);
+        }
+        // the next tile's scores overwrite the A operands read above (MMAs
+        // from one thread run in issue order); its elementwise phase then
+        // overlaps this tile's dQ^T
+        if (!C::EARLY_DP && t + 1 < T && !issue_dp(t + 1)) { ok = false; break; }
+        if (t + 1 < T && !issue_s(t + 1)) { ok = false; break; }
         if (t >= 1) {
           if (!warp_wait(dq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
           tc_fence_after();
         }
+        {
+          const uint32_t k_m = opaque(k_mn), ds_m = opaque(ds_mn);
 #pragma unroll
-        for (int k = 0; k < C::BM / 16; ++k)  // contraction over the 128 keys
-          mma_ss_w(t_dq, k_m + kstep_off(k), ds_m + kstep_off(k), id_dq, k > 0 ? 1u : 0u);
-        mma_commit_w(dq_full);
-        // the next tile's scores overwrite the A operands read above; MMAs
-        // from one thread run in issue order
-        if (t + 1 < T && !issue_scores(t + 1)) { ok = false; break; }
+          for (int k = 0; k < C::BM / 16; ++k)  // contraction over the 128 keys
+            mma_ss_w(t_dq, k_m + kstep_off(k), ds_m + kstep_off(k), id_dq, k > 0 ? 1u : 0u);
+          mma_commit_w(dq_full);
+        }
       }
       if (ok) mma_commit_w(acc_done);
       mma_commit_w(drain);
@@ -638,6 +661,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int j = j0 + row;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sc2 = prm.scale * kLog2e;
+    // dQ^T partial of a finished tile (TMEM lane = feature index, column =
+    // query) into the fp32 accumulator
+    auto drain_dq = [&](int t, uint32_t (&dq)[NC]) -> bool {
+      if (!warp_wait(dq_full, t & 1, abort_flag, prm.status)) return false;
+      tc_fence_after();
+      tmem_ld16(tmem + lane_off + C::T_DQ + NC * slice, dq);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      return true;
+    };
+    auto reduce_dq = [&](int t, const uint32_t (&dq)[NC]) {
+      const int qa = qstart + rotated(t, rot, T) * C::BN + NC * slice;
+      if (D == 128) {
+        float* base = prm.acc + ((size_t)bh * N + qa) * D + row;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(dq[c]) * prm.scale);
+      } else {
+        // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
+        // lanes 32w' + x; the upper 16 lanes of each warp hold nothing
+        if (lane < 16) {
+          float* base = prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane;
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(dq[c]) * prm.scale);
+        }
+      }
+    };
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
@@ -648,6 +699,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t sr[NC], dpr[NC];
       const uint32_t tl = tmem + lane_off + NC * slice;
       tmem_ld16x2(tl + C::T_S, tl + C::T_DP, sr, dpr);
+      if (C::EARLY_DP) {  // the loads above have completed: dP^T is free
+        tc_fence_before();
+        mbar_arrive(sc_read);
+      }
       const float4* sc4 = reinterpret_cast<const float4*>(scal + s * 2 * C::BN + NC * slice);
       const int qa = q0 + NC * slice;
       const bool need_mask = (qa + NC > N) || (j0 + C::BM > N) || (prm.causal && qa < j0 + C::BM);
@@ -679,11 +734,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         body(std::true_type{});
       else
         body(std::false_type{});
-      // A operands of the dV / dK MMAs: bf16 pairs (low half = even query) in
-      // the first 8 of the 16 columns this thread read from S^T and dP^T
-      tmem_st8x2(tl + C::T_S, pw, tl + C::T_DP, dsw);
-      // dS^T also goes to shared memory as the dQ^T B operand; the buffer of
-      // tile t-1 was released by dq_full(t-1), awaited below
+      // A operands of the dV / dK MMAs: bf16 pairs (low half = even query),
+      // P^T in the first 8 and dS^T in the last 8 of the 16 S^T columns this
+      // thread read
+      tmem_st8x2(tl + C::T_S, pw, tl + C::T_S + 8, dsw);
+      // the previous tile's dQ^T MMAs read the dS^T tile below: drain their
+      // result first
+      uint32_t dq[NC];
+      if (t >= 1 && !drain_dq(t - 1, dq)) { ok = false; break; }
+      // dS^T also goes to shared memory as the dQ^T B operand.  This
+      // thread's columns are 16-byte chunks [NC*slice/8, +NC/8) of its row.
 #pragma unroll
       for (int q = 0; q < NC / 8; ++q) {
         const uint32_t chunk = (NC / 8) * slice + q;
@@ -693,28 +753,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(ds_full);
-      // ---- dQ^T partial: TMEM lane = feature index, column = query ----
-      if (!warp_wait(dq_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
-      tc_fence_after();
+      if (t >= 1) reduce_dq(t - 1, dq);
+    }
+    if (ok && T >= 1) {
       uint32_t dq[NC];
-      tmem_ld16(tmem + lane_off + C::T_DQ + NC * slice, dq);
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      if (D == 128) {
-        float* base = prm.acc + ((size_t)bh * N + qa) * D + row;
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-          if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(dq[c]) * prm.scale);
-      } else {
-        // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
-        // lanes 32w' + x; the upper 16 lanes of each warp hold nothing
-        if (lane < 16) {
-          float* base = prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane;
-#pragma unroll
-          for (int c = 0; c < NC; ++c)
-            if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(dq[c]) * prm.scale);
-        }
-      }
+      ok = drain_dq(T - 1, dq);
+      if (ok) reduce_dq(T - 1, dq);
     }
     // ---- epilogue: dK (scaled), dV; each thread D/4 features ----
     ok = __all_sync(0xffffffffu, ok);
