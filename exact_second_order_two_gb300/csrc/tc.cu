@@ -506,15 +506,17 @@ struct Col {
   // inside the 16 columns each thread read: gS^T into the first 8 and dS^T
   // into the last 8 of S^T, gdP^T into the first 8 of G^T.
   static constexpr uint32_t T_S = 0, T_G = 64, T_DP = 128, T_H = 192, T_GK = 256, T_GV = 256 + D;
-  // At d = 128 the next tile's dP^T, H^T are issued as soon as the scores
-  // have been read, so that they run during the elementwise phase.  At d = 64
-  // ([Q|gQ] double-buffered) issuing them after the gradient MMAs measured
-  // faster.
-  static constexpr bool EARLY_DH = D == 128;
+  // The next tile's dP^T, H^T are issued as soon as the scores have been
+  // read, so that they run during the elementwise phase.
+  static constexpr bool EARLY_DH = true;
   // gradQ^T partial (64 columns): its own region when TMEM has room (d = 64),
   // else the S^T columns, which the next tile rewrites last (d = 128)
   static constexpr bool GQ_IN_S = (256 + 2 * D + 64 > 512);
   static constexpr uint32_t T_GQ = GQ_IN_S ? T_S : 256 + 2 * D;
+  // With its own region the gradQ^T MMAs of a tile follow the next tile's
+  // scores, so they run during that tile's elementwise phase, and the
+  // elementwise warps drain the partial one tile late.
+  static constexpr bool LATE_GQ = !GQ_IN_S;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -779,8 +781,6 @@ __global__ void __launch_bounds__(kColThreads, 1)
         const uint32_t q_mn = opaque(lo_mnmajor(qgq_s, 2 * C::BN * 128)),
                        gq_mn = opaque(lo_mnmajor(qgq_s + C::BN * 128, 2 * C::BN * 128));
         const uint32_t do_mn = opaque(lo_mnmajor(sb + C::OFF_DO + ds * C::QB, C::BN * 128));
-        const uint32_t k_m = opaque(k_mn), gk_m = opaque(gk_mn), ds_m = opaque(ds_mn),
-                       gs_m = opaque(gs_mn);
         const uint32_t first = t > 0 ? 1u : 0u;
         // gradK first: it releases the [Q|gQ] stage that the next tile waits for
 #pragma unroll
@@ -793,21 +793,29 @@ __global__ void __launch_bounds__(kColThreads, 1)
         for (int k = 0; k < C::BN / 16; ++k)
           mma_ts_w(t_gv, t_g + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
         mma_commit_w(do_empty + ds);
-        if (!C::GQ_IN_S && t >= 1) {
-          if (!warp_wait(gq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
-          tc_fence_after();
-        }
-        // at d = 128 this overwrites S^T, whose A operands the gradK MMAs
-        // above read first: MMAs from one thread run in issue order
+        // gradQ^T of tile t, once the previous partial has been drained; at
+        // d = 128 it overwrites S^T, whose A operands the gradK MMAs above
+        // read first (MMAs from one thread run in issue order)
+        auto issue_gq = [&]() -> bool {
+          if (!C::GQ_IN_S && t >= 1) {
+            if (!warp_wait(gq_empty, (t - 1) & 1, abort_flag, prm.status)) return false;
+            tc_fence_after();
+          }
+          const uint32_t k_m = opaque(k_mn), gk_m = opaque(gk_mn), ds_m = opaque(ds_mn),
+                         gs_m = opaque(gs_mn);
 #pragma unroll
-        for (int k = 0; k < C::BM / 16; ++k) {  // contraction over the 128 keys
-          mma_ss_w(t_gq, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
-          if (has_gk) mma_ss_w(t_gq, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
-        }
-        mma_commit_w(gq_full);
+          for (int k = 0; k < C::BM / 16; ++k) {  // contraction over the 128 keys
+            mma_ss_w(t_gq, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
+            if (has_gk) mma_ss_w(t_gq, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
+          }
+          mma_commit_w(gq_full);
+          return true;
+        };
+        if (!C::LATE_GQ && !issue_gq()) { ok = false; break; }
         // without EARLY_DH, ds_full (all scores read) has already freed dP^T, H^T
         if (!C::EARLY_DH && t + 1 < T && !issue_dh(t + 1)) { ok = false; break; }
         if (t + 1 < T && !issue_sg(t + 1)) { ok = false; break; }
+        if (C::LATE_GQ && !issue_gq()) { ok = false; break; }
       }
       if (ok) mma_commit_w(acc_done);
       mma_commit_w(drain);
@@ -823,6 +831,32 @@ __global__ void __launch_bounds__(kColThreads, 1)
     const float sc2 = prm.scale * kLog2e;
     const f2 sc2_2 = {sc2, sc2}, scale_2 = {prm.scale, prm.scale};
     const bool has_g = has_gq || has_gk, has_h = has_gv;
+    // gradQ^T partial of tile t (TMEM lane = feature index, column = query),
+    // once gq_full(t) has been awaited
+    auto load_gq = [&](uint32_t (&gq)[NC]) {
+      tc_fence_after();
+      tmem_ld16(tmem + lane_off + C::T_GQ + NC * slice, gq);
+      tc_fence_before();
+      mbar_arrive(gq_empty);  // TMEM region free; the reductions follow
+    };
+    auto reduce_gq = [&](int t, const uint32_t (&gq)[NC]) {
+      const int qa = qstart + rotated(t, rot, T) * C::BN + NC * slice;
+      if (D == 128) {
+        float* base = prm.acc + ((size_t)bh * N + qa) * D + row;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
+      } else {
+        // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
+        // lanes 32w' + x; the upper 16 lanes of each warp hold nothing.
+        if (lane < 16) {
+          float* base = prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane;
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
+        }
+      }
+    };
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
@@ -888,8 +922,14 @@ __global__ void __launch_bounds__(kColThreads, 1)
       // gdP^T in the first 8 it read from G^T; one 16-query contraction step
       // per slice
       tmem_st8x3(tl + C::T_S, gsw, tl + C::T_S + 8, dsw, tl + C::T_G, gdw);
-      // dS^T and gS^T also go to shared memory as the gradQ^T B operands; the
-      // buffers of tile t-1 were released by gq_full(t-1), awaited below.
+      // With LATE_GQ the previous tile's gradQ^T MMAs read the dS^T / gS^T
+      // tiles below: wait for them first (their result stays in TMEM until
+      // gq_empty).  Otherwise that wait ended the previous iteration.
+      if (C::LATE_GQ && t >= 1 && !warp_wait(gq_full, (t - 1) & 1, abort_flag, prm.status)) {
+        ok = false;
+        break;
+      }
+      // dS^T and gS^T also go to shared memory as the gradQ^T B operands.
       // This thread's columns are 16-byte chunks [NC*slice/8, +NC/8) of its row.
 #pragma unroll
       for (int q = 0; q < NC / 8; ++q) {
@@ -902,29 +942,24 @@ __global__ void __launch_bounds__(kColThreads, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(ds_full);
-      // ---- gradQ^T partial: TMEM lane = feature index, column = query ----
-      if (!warp_wait(gq_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
-      tc_fence_after();
       uint32_t gq[NC];
-      tmem_ld16(tmem + lane_off + C::T_GQ + NC * slice, gq);
-      tc_fence_before();
-      mbar_arrive(gq_empty);  // TMEM region free; the reductions follow
-      if (D == 128) {
-        const int dcol = row;
-        float* base = prm.acc + ((size_t)bh * N + qa) * D + dcol;
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-          if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
-      } else {
-        // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
-        // lanes 32w' + x; the upper 16 lanes of each warp hold nothing.
-        if (lane < 16) {
-          const int dcol = 16 * (warp & 3) + lane;
-          float* base = prm.acc + ((size_t)bh * N + qa) * D + dcol;
-#pragma unroll
-          for (int c = 0; c < NC; ++c)
-            if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
+      if (C::LATE_GQ) {
+        if (t >= 1) {
+          load_gq(gq);
+          reduce_gq(t - 1, gq);
         }
+      } else {
+        if (!warp_wait(gq_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+        load_gq(gq);
+        reduce_gq(t, gq);
+      }
+    }
+    if (C::LATE_GQ && ok && T >= 1) {
+      ok = warp_wait(gq_full, (T - 1) & 1, abort_flag, prm.status);
+      if (ok) {
+        uint32_t gq[NC];
+        load_gq(gq);
+        reduce_gq(T - 1, gq);
       }
     }
     // ---- epilogue: gradK (scaled), gradV; each thread D/4 features ----
