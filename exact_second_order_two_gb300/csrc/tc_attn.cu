@@ -52,7 +52,8 @@ constexpr int kFwdCols = 128 / kFwdSlices;          // key columns per thread
 constexpr float kLn2 = 0.6931471805599453f;
 
 // ===========================================================================
-// Forward: row-stationary, two sweeps over the key tiles.
+// Forward: row-stationary, one sweep over the key tiles with an online
+// softmax.
 // ===========================================================================
 template <int D>
 struct Fwd {
@@ -61,20 +62,25 @@ struct Fwd {
   static constexpr uint32_t QB = BM * D * 2;   // stationary Q tile
   static constexpr uint32_t KB = BN * D * 2;   // one streamed K or V tile
   static constexpr uint32_t OFF_Q = 0, OFF_K = QB, OFF_V = OFF_K + KSTAGES * KB;
-  static constexpr uint32_t OFF_PART = OFF_V + VSTAGES * KB;  // [m, l][slices][128]
-  static constexpr uint32_t OFF_MISC = OFF_PART + 2 * kFwdSlices * 128 * 4;
+  // [2][slices][128] per-tile row maxima, then [slices][128] row sums
+  static constexpr uint32_t OFF_RED = OFF_V + VSTAGES * KB;
+  static constexpr uint32_t OFF_MISC = OFF_RED + 3 * kFwdSlices * 128 * 4;
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "forward shared memory budget");
   // TMEM columns: S (two buffers of 128), O, bf16 Q as the A operand of
-  // S = Q K^T.  In the second sweep each elementwise thread writes bf16 P
-  // into the first 16 of the 32 S columns it read: keys 32s + 2c, + 1 of
-  // slice s in column 32s + c, so 16-key step k of P V sits at p_col(k).
+  // S = Q K^T.  Each elementwise thread writes bf16 P over the first 16 of
+  // the 32 S columns it read: keys 32s + 2c, + 1 of slice s in column
+  // 32s + c, so 16-key step k of P V sits at p_col(k).
   static constexpr uint32_t T_O = 256, TMEM_COLS = 512;
   __host__ __device__ static constexpr uint32_t T_S(int b) { return 128u * b; }
   __host__ __device__ static constexpr uint32_t p_col(int k) { return 32u * (k >> 1) + 8u * (k & 1); }
   static constexpr uint32_t T_QA = 256 + D;
   static_assert(T_QA + D / 2 <= TMEM_COLS, "forward TMEM budget");
+  // The running row maximum m (log2 domain) only moves when a tile's maximum
+  // exceeds it by more than kRescale: P = 2^(S c log2 e - m) then stays
+  // below 2^kRescale, and O is rescaled in TMEM only on those rare moves.
+  static constexpr float kRescale = 8.f;
 };
 
 struct FwdParams {
@@ -104,13 +110,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint64_t* v_empty = v_full + C::VSTAGES;       // [VSTAGES]
   uint64_t* s_full = v_empty + C::VSTAGES;       // [2]
   uint64_t* s_empty = s_full + 2;                // [2]: S read out of TMEM
-  uint64_t* p_full = s_empty + 2;                // [2]: bf16 P written over S
-  uint64_t* o_done = p_full + 2;
-  uint64_t* q_tmem = o_done + 1;
+  uint64_t* p_full = s_empty + 2;                // [2]: bf16 P written over S, O rescaled
+  uint64_t* o_ready = p_full + 2;                // one phase per tile: P V MMAs done
+  uint64_t* red_full = o_ready + 1;              // [2]: the slices' tile maxima written
+  uint64_t* q_tmem = red_full + 2;
   uint64_t* drain = q_tmem + 1;
+  static_assert((12 + 2 * C::KSTAGES + 2 * C::VSTAGES) * 8 <= 256,
+                "barriers end below the TMEM slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
-  float* part = reinterpret_cast<float*>(smem + C::OFF_PART);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = prm.N;
@@ -122,7 +131,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int kend = prm.causal ? min(N, i0 + C::BM) : N;
   const int T = (kend + C::BN - 1) / C::BN;
   const int rot = blk % T;
-  const int I = 2 * T;  // sweep 1: iterations [0, T); sweep 2: [T, 2T)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -139,7 +147,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(s_empty + b, kFwdConsumers);
       mbar_init(p_full + b, kFwdConsumers);
     }
-    mbar_init(o_done, 1);
+    mbar_init(o_ready, 1);
+    mbar_init(red_full + 0, kFwdConsumers);
+    mbar_init(red_full + 1, kFwdConsumers);
     mbar_init(q_tmem, kFwdConsumers);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -159,30 +169,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_arrive_expect_tx(q_full, C::QB);
       load_tile(smem + C::OFF_Q, &mQ, q_full, i0, bh);
       int k_issued = 0, v_issued = 0;
-      for (int i = 0; i < I; ++i) {
-        const int s = i % C::KSTAGES;
-        const int kt = rotated(i < T ? i : i - T, rot, T) * C::BN;
-        if (i >= C::KSTAGES &&
-            !wait_bar(k_empty + s, ((i / C::KSTAGES) - 1) & 1, abort_flag, prm.status))
-          break;
+      // K runs ahead of V: S(t) needs K(t) one tile before P V(t) needs V(t)
+      auto load_k = [&](int t) -> bool {
+        const int s = t % C::KSTAGES;
+        if (t >= C::KSTAGES &&
+            !wait_bar(k_empty + s, ((t / C::KSTAGES) - 1) & 1, abort_flag, prm.status))
+          return false;
         mbar_arrive_expect_tx(k_full + s, C::KB);
-        load_tile(smem + C::OFF_K + s * C::KB, &mK, k_full + s, kt, bh);
+        load_tile(smem + C::OFF_K + s * C::KB, &mK, k_full + s, rotated(t, rot, T) * C::BN, bh);
         ++k_issued;
-        if (i >= T) {
-          const int t = i - T, vs = t % C::VSTAGES;
-          if (t >= C::VSTAGES &&
-              !wait_bar(v_empty + vs, ((t / C::VSTAGES) - 1) & 1, abort_flag, prm.status))
-            break;
-          mbar_arrive_expect_tx(v_full + vs, C::KB);
-          load_tile(smem + C::OFF_V + vs * C::KB, &mV, v_full + vs, kt, bh);
-          ++v_issued;
-        }
+        return true;
+      };
+      auto load_v = [&](int t) -> bool {
+        const int s = t % C::VSTAGES;
+        if (t >= C::VSTAGES &&
+            !wait_bar(v_empty + s, ((t / C::VSTAGES) - 1) & 1, abort_flag, prm.status))
+          return false;
+        mbar_arrive_expect_tx(v_full + s, C::KB);
+        load_tile(smem + C::OFF_V + s * C::KB, &mV, v_full + s, rotated(t, rot, T) * C::BN, bh);
+        ++v_issued;
+        return true;
+      };
+      bool pok = load_k(0);
+      for (int t = 0; pok && t < T; ++t) {
+        if (t + 1 < T && !load_k(t + 1)) break;
+        if (!load_v(t)) break;
       }
       // after an abort, loads still in flight must land before the CTA exits
       if (*abort_flag) {
         mbar_wait_bounded(q_full, 0, prm.status, 100000000ull);
-        for (int i = max(0, k_issued - C::KSTAGES); i < k_issued; ++i)
-          mbar_wait_bounded(k_full + (i % C::KSTAGES), (i / C::KSTAGES) & 1, prm.status,
+        for (int t = max(0, k_issued - C::KSTAGES); t < k_issued; ++t)
+          mbar_wait_bounded(k_full + (t % C::KSTAGES), (t / C::KSTAGES) & 1, prm.status,
                             100000000ull);
         for (int t = max(0, v_issued - C::VSTAGES); t < v_issued; ++t)
           mbar_wait_bounded(v_full + (t % C::VSTAGES), (t / C::VSTAGES) & 1, prm.status,
@@ -192,31 +209,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else if (warp == kFwdMmaWarp) {
     {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
       constexpr uint32_t id_s = idesc_bf16(128, C::BN, false, false);  // S = Q K^T: N = BN
-      constexpr uint32_t id_o = idesc_bf16(128, D, false, true);    // O += P V: N = D, B MN
+      constexpr uint32_t id_o = idesc_bf16(128, D, false, true);       // O += P V: N = D, B MN
       const uint32_t t_o = tmem + C::T_O, t_q = tmem + C::T_QA;
       bool ok = warp_wait(q_tmem, 0, abort_flag, prm.status);
-      // O += P(t) V(t), A = bf16 P from TMEM (in the S buffer of iteration
-      // T + t), contraction over the tile's keys
+      // O += P(t) V(t), A = bf16 P from TMEM (in S buffer t & 1), contraction
+      // over the tile's keys; o_ready completes once per tile
       auto issue_pv = [&](int t) -> bool {
         const int pb = t & 1, vs = t % C::VSTAGES;
         if (!warp_wait(p_full + pb, (t >> 1) & 1, abort_flag, prm.status)) return false;
         if (!warp_wait(v_full + vs, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
         tc_fence_after();
         const uint32_t v_mn = opaque(lo_mnmajor(sb + C::OFF_V + vs * C::KB, C::BN * 128));
-        const uint32_t t_p = tmem + C::T_S((T + t) & 1);
+        const uint32_t t_p = tmem + C::T_S(pb);
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
           mma_ts_w(t_o, t_p + C::p_col(k), v_mn + kstep_off(k), id_o, (t > 0 || k > 0) ? 1u : 0u);
         mma_commit_w(v_empty + vs);
+        mma_commit_w(o_ready);
         return true;
       };
-      // S(i) reuses the buffer of iteration i - 2: read out (s_empty) and, in
-      // the second sweep, its P consumed by the P V MMAs of iteration i - 1,
-      // which run before S(i) in issue order
-      for (int i = 0; ok && i < I; ++i) {
-        const int s = i % C::KSTAGES, b = i & 1;
-        if (!warp_wait(k_full + s, (i / C::KSTAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
-        if (i >= 2 && !warp_wait(s_empty + b, ((i >> 1) - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+      // S(t) reuses the buffer of tile t - 2: read out (s_empty) and its P
+      // consumed by the P V MMAs of tile t - 2, issued before S(t)
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t % C::KSTAGES, b = t & 1;
+        if (!warp_wait(k_full + s, (t / C::KSTAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (t >= 2 && !warp_wait(s_empty + b, ((t >> 1) - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_lo = opaque(lo_kmajor(sb + C::OFF_K + s * C::KB));
         const uint32_t t_s = tmem + C::T_S(b);
@@ -225,9 +242,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mma_ts_w(t_s, t_q + 8 * k, k_lo + kslice_off(C::BN, k), id_s, k > 0 ? 1u : 0u);
         mma_commit_w(s_full + b);
         mma_commit_w(k_empty + s);
-        if (i >= T + 1 && !issue_pv(i - T - 1)) { ok = false; break; }
+        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
       }
-      if (ok && issue_pv(T - 1)) mma_commit_w(o_done);
+      if (ok) ok = issue_pv(T - 1);
       // every MMA this thread issued has completed before TMEM is released
       mma_commit_w(drain);
       mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
@@ -263,26 +280,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_before();
       mbar_arrive(q_tmem);
     }
-    // log2-domain running max m2 and sum l = sum_j 2^(S_ij c log2 e - m2)
-    float m2 = -INFINITY, l = 0.f;
-    // S of iteration it (sweep 1: it < T, sweep 2: it >= T) into registers;
-    // false if a wait gave up
-    auto load_s = [&](int it, uint32_t (&sr)[NC]) -> bool {
-      const int b = it & 1;
-      if (!warp_wait(s_full + b, (it >> 1) & 1, abort_flag, prm.status)) return false;
+    // m: the row's reference maximum (log2 domain), the same in all slices;
+    // l: this slice's sum of 2^(S c log2 e - m)
+    float m = -INFINITY, l = 0.f;
+    for (int t = 0; ok && t < T; ++t) {
+      const int b = t & 1;
+      if (!warp_wait(s_full + b, (t >> 1) & 1, abort_flag, prm.status)) { ok = false; break; }
       tc_fence_after();
+      uint32_t sr[NC];
       tmem_ld32(tmem + lane_off + C::T_S(b) + NC * slice, sr);
       tc_fence_before();
       mbar_arrive(s_empty + b);
-      return true;
-    };
-    for (int t = 0; ok && t < T; ++t) {
-      uint32_t sr[NC];
-      if (!load_s(t, sr)) { ok = false; break; }
       const int j0 = rotated(t, rot, T) * C::BN + NC * slice;
       const bool need_mask = !row_ok || (j0 + NC > N) || (prm.causal && j0 + NC - 1 > i);
-      // raw maximum first (c log2 e > 0 preserves the order); masked
-      // entries become -inf, which the sum below turns into 2^-inf = 0
+      // this slice's raw maximum (c log2 e > 0 keeps the order); masked
+      // entries become -inf, so they give 2^-inf = 0 below
       float mx = -INFINITY;
       if (need_mask) {
 #pragma unroll
@@ -297,75 +309,79 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < NC; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
       }
-      mx *= sc2;
-      if (mx > m2) {
-        l *= ex2_approx(m2 - mx);  // 2^(-inf) = 0 on the first update
-        m2 = mx;
+      // the row's maximum over the tile, through shared memory and a bounded
+      // wait on an mbarrier (one buffer per tile parity: a buffer is
+      // rewritten only after every thread has arrived for the next tile,
+      // hence after it read this one)
+      float* rt = red + b * NS * 128;
+      rt[slice * 128 + row] = mx * sc2;
+      mbar_arrive(red_full + b);
+      if (!warp_wait(red_full + b, (t >> 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < NS; ++u) mt = fmaxf(mt, rt[u * 128 + row]);
+      // the reference maximum moves (the same decision in every slice of a
+      // row; rows, i.e. lanes, decide independently)
+      const bool move = mt > m + C::kRescale;
+      const float alpha = move ? ex2_approx(m - mt) : 1.f;  // 0 while m is still -inf
+      l *= alpha;
+      // O (this slice's D/NS columns of the row) holds the P V sums of the
+      // earlier tiles: rescale it once their MMAs are done.  The wait and the
+      // TMEM accesses are warp-collective, so the whole warp takes this
+      // branch when any lane needs it; the other lanes scale by 1.
+      const bool scale_o = move && t >= 1 && m > -INFINITY;
+      if (__any_sync(0xffffffffu, scale_o)) {
+        if (!warp_wait(o_ready, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+        tc_fence_after();
+        const float f = scale_o ? alpha : 1.f;
+        constexpr int PART = D / NS;
+#pragma unroll
+        for (int cc = 0; cc < PART; cc += 16) {
+          uint32_t v[16];
+          const uint32_t ta = tmem + lane_off + C::T_O + PART * slice + cc;
+          tmem_ld16(ta, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
+          tmem_st16(ta, v);
+        }
       }
-      if (m2 > -INFINITY) {
-        const f2 nm = {-m2, -m2};
+      if (move) m = mt;
+      uint32_t pw[NC / 2];
+      if (m > -INFINITY) {
+        const f2 nm = {-m, -m};
         f2 acc = {0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < NC; c += 2) {
           const f2 x = fma2({__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, sc2_2, nm);
-          acc = add2(acc, f2{ex2_approx(x.x), ex2_approx(x.y)});
+          const f2 p = {ex2_approx(x.x), ex2_approx(x.y)};
+          acc = add2(acc, p);
+          pw[c >> 1] = pack_bf16(p.x, p.y);
         }
         l += acc.x + acc.y;
+      } else {
+#pragma unroll
+        for (int c = 0; c < NC / 2; ++c) pw[c] = 0u;
       }
-    }
-    // combine the column slices of each row (every consumer thread gets here,
-    // also after a failed wait, so the barrier cannot hang)
-    part[slice * 128 + row] = m2;
-    part[(NS + slice) * 128 + row] = l;
-    named_sync<kFwdConsumers>(1);
-    float lse2;
-    {
-      float M = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < NS; ++u) M = fmaxf(M, part[u * 128 + row]);
-      float L = 0.f;
-#pragma unroll
-      for (int u = 0; u < NS; ++u) {
-        const float mu = part[u * 128 + row];
-        L += mu > -INFINITY ? part[(NS + u) * 128 + row] * ex2_approx(mu - M) : 0.f;
-      }
-      lse2 = (M > -INFINITY && L > 0.f) ? M + log2f(L) : 0.f;
-    }
-    for (int t = 0; ok && t < T; ++t) {
-      uint32_t sr[NC];
-      if (!load_s(T + t, sr)) { ok = false; break; }
-      const int j0 = rotated(t, rot, T) * C::BN + NC * slice;
-      const bool need_mask = !row_ok || (j0 + NC > N) || (prm.causal && j0 + NC - 1 > i);
-      uint32_t pw[NC / 2];
-      auto body = [&](auto masked) {
-        const f2 nl = {-lse2, -lse2};
-#pragma unroll
-        for (int c = 0; c < NC; c += 2) {
-          const f2 x = fma2({__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])}, sc2_2, nl);
-          float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          if (decltype(masked)::value) {
-            const int j = j0 + c;
-            p0 = (row_ok && j < N && (!prm.causal || j <= i)) ? p0 : 0.f;
-            p1 = (row_ok && j + 1 < N && (!prm.causal || j + 1 <= i)) ? p1 : 0.f;
-          }
-          pw[c >> 1] = pack_bf16(p0, p1);
-        }
-      };
-      if (need_mask)
-        body(std::true_type{});
-      else
-        body(std::false_type{});
       // bf16 P over the first 16 of the 32 S columns this thread read: keys
       // NC*slice + 2c, + 1 in column NC*slice + c (two 16-key MMA steps)
-      tmem_st16(tmem + lane_off + C::T_S((T + t) & 1) + NC * slice, pw);
+      tmem_st16(tmem + lane_off + C::T_S(b) + NC * slice, pw);
       tc_fence_before();
-      mbar_arrive(p_full + (t & 1));
+      mbar_arrive(p_full + b);
     }
-    // ---- epilogue: O (bf16) and LSE (natural log) ----
+    // ---- epilogue: O / l (bf16) and LSE (natural log) ----
+    // the slices' sums share the reference maximum m; every consumer thread
+    // gets to this barrier, also after a failed wait
+    float* part = red + 2 * NS * 128;
+    part[slice * 128 + row] = l;
+    named_sync<kFwdConsumers>(1);
+    float L = 0.f;
+#pragma unroll
+    for (int u = 0; u < NS; ++u) L += part[u * 128 + row];
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) ok = warp_wait(o_done, 0, abort_flag, prm.status);
+    if (ok) ok = warp_wait(o_ready, (T - 1) & 1, abort_flag, prm.status);
     tc_fence_after();
     if (ok) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
       constexpr int PART = D / NS;  // output features per thread
       uint4* op = reinterpret_cast<uint4*>(prm.o + srow * D + PART * slice);
 #pragma unroll
@@ -376,13 +392,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int q = 0; q < 2; ++q)
             op[cc / 8 + q] = make_uint4(
-                pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                pack_bf16(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                pack_bf16(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                pack_bf16(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                pack_bf16(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
         }
       }
-      if (slice == 0 && row_ok) prm.lse[srow] = lse2 * kLn2;
+      if (slice == 0 && row_ok) prm.lse[srow] = (m > -INFINITY && L > 0.f) ? (m + log2f(L)) * kLn2 : 0.f;
     }
   }
   tc_fence_before();

@@ -66,6 +66,11 @@ SMALL = [
     ("bf16_d128_nc",   1, 1, 129, 128, "bf16", False),
     ("bf16_d40",       1, 2,  77,  40, "bf16", True),
     ("bf16_d128_long", 1, 1, 1000, 128, "bf16", True),
+    # several key blocks and query tiles without the mask, a ragged last
+    # 128-key forward tile (1000 = 7*128 + 104) and two (batch, head) units
+    ("bf16_d128_nc_long", 1, 2, 1000, 128, "bf16", False),
+    ("bf16_d64_nc_long",  2, 1, 1000, 64, "bf16", False),
+    ("bf16_d64_long",     1, 1, 1000, 64, "bf16", True),
 ]
 
 
