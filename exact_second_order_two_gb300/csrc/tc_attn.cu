@@ -6,20 +6,22 @@
 //   dP = dO V^T,  D_i = dO_i . O_i,  dS = P*(dP - D),
 //   dQ = c dS K,  dK = c dS^T Q,  dV = P^T dO.
 //
-// forward (row-stationary, 128 query rows per CTA, 128-key tiles): two
-//   sweeps over the key tiles.  The first reduces each row's log-sum-exp from
-//   S in TMEM (running max and sum in registers); the second forms the exactly
-//   normalised P = exp(S - LSE) in bf16, in place of S in TMEM, and
-//   accumulates O += P V there.  O never needs rescaling, at the price of S
-//   computed twice.
+// forward (row-stationary, 128 query rows per CTA, 128-key tiles): one sweep
+//   over the key tiles with an online softmax.  S goes into TMEM; bf16
+//   P = 2^(S c log2 e - m) is written over it and O += P V accumulates in
+//   TMEM.  The reference maximum m moves only when a tile's maximum exceeds
+//   it by more than 8 (log2 units), and O is then rescaled in TMEM; the
+//   epilogue divides by the row sum and writes LSE.
 // first backward (key-stationary, 128 key rows per CTA, 64-query tiles):
-//   S^T and dP^T into TMEM; bf16 P^T and dS^T written back into TMEM as the
-//   A operands of dV += P^T dO and dK += dS^T Q; dQ^T partial = K^T dS^T
-//   reduced into an fp32 accumulator, then converted.
+//   S^T and dP^T into TMEM; bf16 P^T and dS^T written back into the S^T
+//   columns as the A operands of dV += P^T dO and dK += dS^T Q; the next
+//   tile's scores are issued before this tile's dQ^T = K^T dS^T, which is
+//   reduced into an fp32 accumulator one tile late, then converted.
 //
 // Warp roles as in the BoB kernels: elementwise warps own TMEM lanes, one TMA
-// producer warp, one MMA warp (TMEM allocator, single-thread issuer).  Every
-// wait is bounded.
+// producer warp, one MMA warp (TMEM allocator; elect.sync picks the issuing
+// lane).  Every mbarrier wait is bounded, and every warp-collective operation
+// sits in warp-uniform control flow.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
