@@ -789,10 +789,6 @@ __global__ void __launch_bounds__(kColThreads, 1)
           if (has_gq) mma_ts_w(t_gk, t_s + 16 * k + 8, gq_mn + kstep_off(k), id_out, 1u);
         }
         mma_commit_w(qg_empty + s);
-#pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts_w(t_gv, t_g + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-        mma_commit_w(do_empty + ds);
         // gradQ^T of tile t, once the previous partial has been drained; at
         // d = 128 it overwrites S^T, whose A operands the gradK MMAs above
         // read first (MMAs from one thread run in issue order)
@@ -811,7 +807,13 @@ __global__ void __launch_bounds__(kColThreads, 1)
           mma_commit_w(gq_full);
           return true;
         };
+        // at d = 128 gradQ^T goes before gradV: its partial is drained sooner,
+        // and the next tile's scores wait for that drain
         if (!C::LATE_GQ && !issue_gq()) { ok = false; break; }
+#pragma unroll
+        for (int k = 0; k < C::BN / 16; ++k)
+          mma_ts_w(t_gv, t_g + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+        mma_commit_w(do_empty + ds);
         // without EARLY_DH, ds_full (all scores read) has already freed dP^T, H^T
         if (!C::EARLY_DH && t + 1 < T && !issue_dh(t + 1)) { ok = false; break; }
         if (t + 1 < T && !issue_sg(t + 1)) { ok = false; break; }

@@ -563,12 +563,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) break;
       // the stage's scalars were last read by the elementwise warps of tile
-      // t - STAGES, which finished before the dK MMAs that freed the stage
+      // t - STAGES, which finished before the dK MMAs that freed the stage;
+      // stored negated, since both are subtracted
       float* sc = scal + s * 2 * C::BN;
 #pragma unroll
       for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = pre[a][u];
+        for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = -pre[a][u];
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full + s, C::QB);
@@ -679,6 +680,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int j = j0 + row;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float sc2 = prm.scale * kLog2e;
+    const f2 sc2_2 = {sc2, sc2};
     // dQ^T partial of a finished tile (TMEM lane = feature index, column =
     // query) into the fp32 accumulator
     auto drain_dq = [&](int t, uint32_t (&dq)[NC]) -> bool {
@@ -727,25 +729,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t pw[NC / 2], dsw[NC / 2];
       auto body = [&](auto masked) {
 #pragma unroll
-        for (int c4 = 0; c4 < NC / 4; ++c4) {
+        for (int c4 = 0; c4 < NC / 4; ++c4) {  // 4 query columns per step
+          // negated row scalars of the 4 queries: -LSE log2 e, -D
           const float4 L = sc4[c4], Dd = sc4[C::BN / 4 + c4];
-          const float lv[4] = {L.x, L.y, L.z, L.w}, dv[4] = {Dd.x, Dd.y, Dd.z, Dd.w};
-          float o_p[4], o_ds[4];
+          const f2 nl[2] = {{L.x, L.y}, {L.z, L.w}}, nd[2] = {{Dd.x, Dd.y}, {Dd.z, Dd.w}};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int cc = 4 * c4 + e;
-            float p = ex2_approx(__uint_as_float(sr[cc]) * sc2 - lv[e]);
+          for (int hh = 0; hh < 2; ++hh) {  // query columns cc, cc + 1: one packed pair
+            const int cc = 4 * c4 + 2 * hh;
+            const f2 x = fma2({__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])}, sc2_2, nl[hh]);
+            f2 p = {ex2_approx(x.x), ex2_approx(x.y)};
             if (decltype(masked)::value) {
               const int q = qa + cc;
-              p = (q < N && j < N && (!prm.causal || q >= j)) ? p : 0.f;
+              p.x = (q < N && j < N && (!prm.causal || q >= j)) ? p.x : 0.f;
+              p.y = (q + 1 < N && j < N && (!prm.causal || q + 1 >= j)) ? p.y : 0.f;
             }
-            o_p[e] = p;
-            o_ds[e] = p * (__uint_as_float(dpr[cc]) - dv[e]);
+            const f2 ds = mul2(p, add2({__uint_as_float(dpr[cc]), __uint_as_float(dpr[cc + 1])}, nd[hh]));
+            pw[cc >> 1] = pack_bf16(p.x, p.y);
+            dsw[cc >> 1] = pack_bf16(ds.x, ds.y);
           }
-          pw[2 * c4] = pack_bf16(o_p[0], o_p[1]);
-          pw[2 * c4 + 1] = pack_bf16(o_p[2], o_p[3]);
-          dsw[2 * c4] = pack_bf16(o_ds[0], o_ds[1]);
-          dsw[2 * c4 + 1] = pack_bf16(o_ds[2], o_ds[3]);
         }
       };
       if (need_mask)
