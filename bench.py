@@ -316,11 +316,17 @@ def run_ours(args, w, rank, world, dist):
         per_kernel.append((name, products, t))
     dom = max(per_kernel, key=lambda x: x[2])
     peaks = load_peaks()
-    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    # The timed region is well under a minute of back-to-back calls, not the
+    # seconds-long power-capped loop the sustained figure comes from, so the
+    # kernel is held to the burst peak; the sustained fraction is printed too.
+    peak = peaks["bf16_tflops"]
+    sustained = peaks.get("bf16_tflops_sustained", peak)
     achieved = flops_bob(w, dom[1]) / (dom[2] * 1e-3) / 1e12 if dom[1] else 0.0
+    peak_mem = torch.cuda.max_memory_allocated(dev)
 
     # end to end through the public API with pinned host buffers
-    e2e = run_e2e(args, w, host, o, lse, outs, ws, call_api=fbob.bob, dev=dev)
+    e2e = None if args.no_e2e else run_e2e(args, w, host, o, lse, outs, ws,
+                                           call_api=fbob.bob, dev=dev)
 
     if rank != 0:
         return
@@ -340,9 +346,10 @@ def run_ours(args, w, rank, world, dist):
         "kernels_ms": {n: t for n, _, t in per_kernel},
         "roofline": {"bound": "tensor", "kernel": dom[0], "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_kind": f"bf16 dense sustained ({peaks.get('source')})",
-                     "frac_of_burst": achieved / peaks["bf16_tflops"],
+                     "peak_kind": f"bf16 dense burst ({peaks.get('source')})",
+                     "frac_of_sustained": achieved / sustained,
                      "traffic": recorded_traffic(dom[0], w.name)},
+        "peak_mem_gib": peak_mem / 2**30,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -422,6 +429,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (profiling runs: fewer launches and "
+                         "no second set of device buffers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

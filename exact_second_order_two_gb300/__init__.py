@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     last_launch_count,
     lib,
     make_shape,
+    noalloc_status,
     path,
     selftest_wait_timeout,
     set_profile_events,

@@ -62,6 +62,7 @@ _SIGNATURES = {
     "fbob_last_launch_count": (ctypes.c_int, []),
     "fbob_selftest_wait_timeout": (ctypes.c_int, [_P, _SZ, ctypes.c_int, _P]),
     "fbob_bob_noalloc": (ctypes.c_int, [_SHP] + [_P] * 13 + [_P]),
+    "fbob_noalloc_status": (ctypes.c_int, [_P]),
 }
 
 
@@ -229,6 +230,14 @@ def bob_noalloc(q, k, v, o, lse, do, gq, gk, gv, causal: bool = False,
                                   *(_ptr(t) for t in outs), _stream(q.device)),
            "fbob_bob_noalloc")
     return tuple(outs)
+
+
+def noalloc_status(device=None) -> int:
+    """Device-side status of the last ``bob_noalloc`` call on ``device``
+    (synchronises that device's current stream)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        return int(lib().fbob_noalloc_status(_stream(dev)))
 
 
 def selftest_wait_timeout(workspace: torch.Tensor, limit_us: int) -> int:

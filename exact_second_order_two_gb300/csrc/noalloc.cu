@@ -14,7 +14,9 @@
 // library keeps FBOB_NOALLOC_SCRATCH_BYTES of its memory reserved until the
 // process exits.  In host code the variable's name is only a host-side
 // stand-in: its device address is fetched once per device with
-// cudaGetSymbolAddress, on the first call made while that device is current.
+// cudaGetSymbolAddress, on the first call made while that device is current,
+// and kept for the life of the process (a device reset, which can move the
+// array, is not supported).
 #include <cuda_runtime.h>
 #include <mutex>
 
@@ -62,4 +64,12 @@ extern "C" int fbob_bob_noalloc(const fbob_shape_t* shape, const void* q, const 
   // from an earlier call do not leak into this one.
   return fbob_bob(shape, q, k, v, o, lse, dO, gq, gk, gv, gradq, gradk, gradv, graddo, scratch,
                   (size_t)FBOB_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+// The status word that device-side bounded waits write sits at the start of
+// the scratch array, where the caller cannot read it: this returns it.
+extern "C" int fbob_noalloc_status(void* stream) {
+  void* scratch = scratch_for_current_device();
+  if (!scratch) return FBOB_ERR_CUDA;
+  return fbob_status(scratch, stream);
 }

@@ -60,6 +60,14 @@ WORKLOADS = {
                  True, 1.5, 0.1, 0.1),
         Workload("bf16_causal_h4_n262144_d64", 1, 4, 262144, 64, "bf16", True,
                  1.0, 1.0, 0.1),
+        # without the causal mask, at the length where dense BoB is stated
+        # to fail and at the two longest lengths
+        Workload("bf16_h4_n16384_d128", 1, 4, 16384, 128, "bf16", False,
+                 1.0, 1.0, 0.1),
+        Workload("bf16_h8_n65536_d128", 1, 8, 65536, 128, "bf16", False,
+                 1.0, 1.0, 0.1),
+        Workload("bf16_h4_n262144_d64", 1, 4, 262144, 64, "bf16", False,
+                 1.0, 1.0, 0.1),
         # profiling-sized cases (inputs still larger than L2 in total)
         Workload("bf16_causal_h8_n8192_d128", 1, 8, 8192, 128, "bf16", True,
                  1.0, 1.0, 0.1),

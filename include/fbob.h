@@ -146,14 +146,22 @@ int fbob_bob(const fbob_shape_t* shape, const void* q, const void* k,
  * array, so calls that can overlap on the GPU (different streams, or host
  * threads) race on it: serialise them.  Each call clears what must start at
  * zero, so contents left by an earlier call do not affect the result.  The
- * status word that device-side bounded waits write lives in that array, out
- * of the caller's reach: check the return code and the stream's error state
- * instead of fbob_status(). */
+ * status word that device-side bounded waits write lives in that array:
+ * read it with fbob_noalloc_status(), not fbob_status().  The array's
+ * address is kept for the life of the process, so calls after a device
+ * reset (cudaDeviceReset) are not supported. */
 int fbob_bob_noalloc(const fbob_shape_t* shape, const void* q, const void* k,
                      const void* v, const void* o, const float* lse,
                      const void* dO, const void* gq, const void* gk,
                      const void* gv, void* gradq, void* gradk, void* gradv,
                      void* graddo, void* stream);
+
+/* Status of the last fbob_bob_noalloc call on the current device: synchronises
+ * `stream` (the stream that call used), then returns the first device-side
+ * error it recorded in the scratch array's status word (FBOB_OK if none), or
+ * FBOB_ERR_CUDA if the stream reports an error or the array cannot be reached.
+ * Like fbob_bob_noalloc, it has no counterpart in the paper. */
+int fbob_noalloc_status(void* stream);
 
 /* Synchronises `stream`, then returns the first error recorded in the
  * workspace's status word by the last call that used `ws` (FBOB_OK if none),

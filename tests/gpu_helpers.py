@@ -22,17 +22,33 @@ def to64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def rel_err(got, ref, floor: float = 1e-2) -> float:
-    """max|got - ref| / max|ref|.  Outputs that are identically zero in exact
-    arithmetic (e.g. dQ at N = 1) leave only rounding noise of cancelled
-    O(1..10) terms; the denominator is floored at ``floor`` (far below the
-    O(0.1..10) magnitude of every non-zero output on these inputs) so such
-    cases compare absolute error against that floor instead of dividing by
-    zero."""
+def rel_err(got, ref, floor: float | None = None) -> float:
+    """max|got - ref| / max|ref| over the compared elements.
+
+    There is no absolute floor by default: the error of every compared set is
+    measured against that set's own largest reference value, so an output
+    that is small everywhere (late key columns under a causal mask, say) is
+    held to the same relative tolerance as a large one, and a zero or a
+    perturbed output fails.  ``floor`` is only for sets that are exactly zero
+    in exact arithmetic (gradQ and gradK at N = 1, causal row 0), where only
+    rounding noise of cancelled terms is left; the caller then passes the
+    scale that noise is measured against."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    denom = max(float(np.max(np.abs(ref))), floor)
+    denom = float(np.max(np.abs(ref))) if ref.size else 0.0
+    if floor is not None:
+        denom = max(denom, floor)
+    if denom == 0.0:
+        raise ValueError("reference is identically zero: pass the floor its "
+                         "rounding noise is measured against")
     return float(np.max(np.abs(got - ref)) / denom)
+
+
+def compare_sampled(got: dict, ref: dict, tol: float) -> dict:
+    """Relative errors of sampled output sets (each set against its own
+    max|ref|); returns {name: error} for the sets above ``tol``."""
+    errs = {name: rel_err(got[name], ref[name]) for name in ref}
+    return {name: e for name, e in errs.items() if not e <= tol}
 
 
 def gpu_pipeline(ins: dict, w: Workload, device="cuda"):
@@ -98,6 +114,53 @@ def invariant_residuals(gpu: dict):
         col_scale = torch.sqrt((g * g).sum(dim=2))
         res["I4_" + name] = (col_sum.abs() / col_scale.clamp_min(1e-30)).max().item()
     return res
+
+
+# Full-size samples.  Row-local outputs (O, LSE, dQ, gradQ, graddO) are
+# compared on random query rows plus rows 0, N/2 and N - 1.  Key-side outputs
+# (dK, dV, gradK, gradV) are compared on a block of key columns chosen to
+# carry real gradient and to run pass 2's long query loops (key block 0 is
+# seen by every query; a mid block by half of them), plus the last columns
+# (the shortest loops) as a set of their own.  Each set is measured against
+# its own max|ref|: there is no absolute floor.  The oracle's cost for a key
+# block is that of every query row that sees it, so the blocks at N >= 65536
+# sit where a few thousand queries see them.
+#   workload: (rows sampled, [(b, h, first key column, key columns)], tail)
+FULL_SIZE_SAMPLES = {
+    "bf16_causal_b2h16_n16384_d128": (24, [(0, 0, 0, 128), (1, 15, 8256, 64)], 64),
+    "bf16_causal_peaked_h8_n65536_d128": (16, [(0, 3, 65536 - 4096, 128)], 64),
+    "bf16_causal_h4_n262144_d64": (12, [(0, 1, 262144 - 1152, 64)], 32),
+    # no mask: every query sees every key, so one block (across the key
+    # block boundary at 8192) costs a full head
+    "bf16_h4_n16384_d128": (16, [(0, 2, 8192 - 32, 64)], 0),
+}
+
+
+def oracle_sample(x, w: Workload, rows, cols):
+    """fp64 oracle values of every output at query rows ``rows`` and key
+    columns ``cols`` of one (batch, head) slice ``x``."""
+    args = (x["q"], x["k"], x["v"], x["do"], x["gq"], x["gk"], x["gv"], w.causal, w.scale)
+    fb = (x["q"], x["k"], x["v"])
+    ref = {}
+    if len(rows):
+        ref["gradq"], ref["graddo"] = oracle.bob_rows(*args, rows)
+        ref["o"], ref["lse"] = oracle.forward_rows(*fb, w.causal, w.scale, rows)
+        ref["dq"] = oracle.backward_rows(*fb, x["do"], w.causal, w.scale, rows)
+    if len(cols):
+        ref["gradk"], ref["gradv"] = oracle.bob_cols(*args, cols)
+        ref["dk"], ref["dv"] = oracle.backward_cols(*fb, x["do"], w.causal, w.scale, cols)
+    return ref
+
+
+def gpu_sample(gpu: dict, b: int, h: int, rows, cols):
+    got = {}
+    for k in ("gradq", "graddo", "o", "dq", "lse"):
+        if len(rows):
+            got[k] = to64(gpu[k][b, h])[rows]
+    for k in ("gradk", "gradv", "dk", "dv"):
+        if len(cols):
+            got[k] = to64(gpu[k][b, h])[cols]
+    return got
 
 
 def sample_rows(N: int, count: int, seed: int) -> np.ndarray:
