@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     path,
     selftest_wait_timeout,
     set_profile_events,
+    set_wait_limit,
     shape_of,
     status,
     workspace_size,

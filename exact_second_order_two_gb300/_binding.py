@@ -63,6 +63,7 @@ _SIGNATURES = {
     "fbob_selftest_wait_timeout": (ctypes.c_int, [_P, _SZ, ctypes.c_int, _P]),
     "fbob_bob_noalloc": (ctypes.c_int, [_SHP] + [_P] * 13 + [_P]),
     "fbob_noalloc_status": (ctypes.c_int, [_P]),
+    "fbob_set_wait_limit": (ctypes.c_longlong, [ctypes.c_longlong]),
 }
 
 
@@ -230,6 +231,15 @@ def bob_noalloc(q, k, v, o, lse, do, gq, gk, gv, causal: bool = False,
                                   *(_ptr(t) for t in outs), _stream(q.device)),
            "fbob_bob_noalloc")
     return tuple(outs)
+
+
+def set_wait_limit(ns: int) -> int:
+    """Limit of one device-side bounded wait in nanoseconds (0 = the 2 s
+    default).  Returns the previous limit."""
+    old = int(lib().fbob_set_wait_limit(int(ns)))
+    if old < 0:
+        raise ValueError(f"wait limit {ns} ns is out of range")
+    return old
 
 
 def noalloc_status(device=None) -> int:

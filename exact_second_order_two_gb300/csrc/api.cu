@@ -12,6 +12,10 @@ namespace fbob {
 namespace {
 
 int g_force_path = -1;
+// 2 s: far above any legitimate wait inside a kernel (microseconds), far
+// below anything that would look like a hang.
+constexpr long long kDefaultWaitLimitNs = 2000000000ll;
+long long g_wait_limit_ns = kDefaultWaitLimitNs;
 cudaEvent_t g_events[16];
 int g_event_count = 0;
 int g_last_launches = 0;
@@ -107,6 +111,8 @@ bool opt_ptrs_ok(std::initializer_list<const void*> ps) {
 
 }  // namespace
 
+unsigned long long wait_limit_ns() { return (unsigned long long)g_wait_limit_ns; }
+
 void LaunchLog::mark() {
   ++launches;
   if (launches < g_event_count) cudaEventRecord(g_events[launches], stream);
@@ -162,6 +168,14 @@ int fbob_set_profile_events(void* const* events, int count) {
 }
 
 int fbob_last_launch_count(void) { return g_last_launches; }
+
+long long fbob_set_wait_limit(long long ns) {
+  const long long old = g_wait_limit_ns;
+  if (ns == 0) g_wait_limit_ns = kDefaultWaitLimitNs;
+  else if (ns > 0 && ns <= 60000000000ll) g_wait_limit_ns = ns;
+  else return -1;
+  return old;
+}
 
 int fbob_forward(const fbob_shape_t* shape, const void* q, const void* k,
                  const void* v, void* o, float* lse, void* ws_ptr,

@@ -61,6 +61,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, but a thread that finds the phase incomplete may be
+// suspended for up to `hint_ns` nanoseconds; it is woken as soon as the
+// phase completes, so a waiting warp sleeps instead of spinning on the
+// barrier and leaves its issue slots to the other warps of its SM
+// sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for phase `parity` of `bar` to complete.  Spins on try_wait
 // (which itself suspends for a hardware-chosen interval), checks the global
 // timer every 64 tries, and gives up after `limit_ns`, recording
@@ -81,10 +99,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar,
     }
   }
 }
-
-// Default limit of one bounded wait: far above any legitimate wait inside a
-// kernel (microseconds), far below anything that would look like a hang.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -59,14 +59,18 @@ cudaError_t tc_backward(const Problem& p, const void* q, const void* k,
                         const void* v, const void* o, const float* lse,
                         const void* dO, void* dq, void* dk, void* dv,
                         const Workspace& ws, LaunchLog& log);
-// fp32 accumulator [elems] -> bf16 output (elems a multiple of 8).
-cudaError_t launch_acc_to_bf16(const float* acc, void* out, size_t elems,
+// scale * fp32 accumulator [elems] -> bf16 output (elems a multiple of 8).
+cudaError_t launch_acc_to_bf16(const float* acc, void* out, size_t elems, float scale,
                                LaunchLog& log);
 cudaError_t tc_bob(const Problem& p, const void* q, const void* k,
                    const void* v, const void* o, const float* lse,
                    const void* dO, const void* gq, const void* gk,
                    const void* gv, void* gradq, void* gradk, void* gradv,
                    void* graddo, const Workspace& ws, LaunchLog& log);
+
+// Limit of one device-side bounded wait, in nanoseconds (process-wide;
+// fbob_set_wait_limit).  Every tensor-core kernel receives it as an argument.
+unsigned long long wait_limit_ns();
 
 // Failure-detection self-test kernel (bounded wait that must run out).
 cudaError_t launch_wait_timeout_selftest(int* status, long long limit_ns,

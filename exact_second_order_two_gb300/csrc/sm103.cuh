@@ -389,35 +389,12 @@ __device__ __forceinline__ void keep16(const uint32_t (&w)[16]) {
 }
 
 // Packed fp32 pairs (sm_100 family f32x2 arithmetic): two lanes of work per
-// instruction, each rounded to nearest as the scalar forms are.
-struct f2 {
-  float x, y;
-};
-__device__ __forceinline__ uint64_t f2_bits(f2 a) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
-  return r;
-}
-__device__ __forceinline__ f2 f2_of(uint64_t r) {
-  f2 a;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
-  return a;
-}
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
-  return f2_of(r);
-}
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return f2_of(r);
-}
-__device__ __forceinline__ f2 add2(f2 a, f2 b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return f2_of(r);
-}
+// instruction, each rounded to nearest as the scalar forms are.  The CUDA
+// float2 builtins leave the register pairing to the compiler.
+using f2 = float2;
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ f2 add2(f2 a, f2 b) { return __fadd2_rn(a, b); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);

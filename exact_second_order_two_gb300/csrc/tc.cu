@@ -118,7 +118,9 @@ struct RowParams {
   float* D_out;
   float* acc_zero;  // fp32 gradQ accumulator rows to clear (may be null)
   int* status;
+  unsigned long long wait_ns;  // limit of one bounded wait
   int N, causal;
+  int BH, G;  // batch * heads, heads per CTA group (cta_coord)
   float scale;
   // which cotangents are present (an absent one is zero: its loads and MMAs
   // are skipped); at least one is
@@ -154,15 +156,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_tmem = w_done + 2;                  // Q, gQ copied into TMEM
   uint64_t* drain = w_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
+  Abort* abort_st = reinterpret_cast<Abort*>(smem + C::OFF_MISC + 264);
   float* part = reinterpret_cast<float*>(smem + C::OFF_PART);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = prm.N;
-  const int bh = blockIdx.y;
+  const int nblk = (prm.N + C::BM - 1) / C::BM;
+  const CtaCoord cc = cta_coord(prm.BH, prm.G, nblk);
+  const int bh = cc.bh;
   // heavy (late) row blocks first under a causal mask
-  const int nblk = gridDim.x;
-  const int blk = prm.causal ? (nblk - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int blk = prm.causal ? (nblk - 1 - cc.blk) : cc.blk;
   const int i0 = blk * C::BM;
   const int kend = prm.causal ? min(N, i0 + C::BM) : N;
   const int T = (kend + C::BN - 1) / C::BN;
@@ -185,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(w_done, 1);
     mbar_init(drain, 1);
     mbar_init(q_tmem, kConsumers);
-    *abort_flag = 0;
+    abort_st->flag = 0;
+    abort_st->limit_ns = prm.wait_ns;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_kg = [&](int t) -> bool {
         const int s = t % C::STAGES;
         if (t >= C::STAGES &&
-            !wait_bar(kg_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status))
+            !wait_bar(kg_empty + s, ((t / C::STAGES) - 1) & 1, abort_st, prm.status))
           return false;
         uint8_t* st = smem + C::OFF_KG + s * C::SB;
         mbar_arrive_expect_tx(kg_full + s, has_gk ? C::SB : C::SB / 2);
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_v = [&](int t) -> bool {
         const int s = t % C::VSTAGES;
         if (t >= C::VSTAGES &&
-            !wait_bar(v_empty + s, ((t / C::VSTAGES) - 1) & 1, abort_flag, prm.status))
+            !wait_bar(v_empty + s, ((t / C::VSTAGES) - 1) & 1, abort_st, prm.status))
           return false;
         uint8_t* st = smem + C::OFF_V + s * C::SB;
         mbar_arrive_expect_tx(v_full + s, has_gv ? C::SB : C::KB);
@@ -237,34 +241,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t + 1 < T && !load_kg(t + 1)) break;
         if (!load_v(t)) break;
       }
-      // after an abort, loads still in flight must land before the CTA exits
-      if (*abort_flag) {
-        mbar_wait_bounded(q_full, 0, prm.status, 100000000ull);
-        for (int t = max(0, kg_issued - C::STAGES); t < kg_issued; ++t)
-          mbar_wait_bounded(kg_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
-                            100000000ull);
-        for (int t = max(0, v_issued - C::VSTAGES); t < v_issued; ++t)
-          mbar_wait_bounded(v_full + (t % C::VSTAGES), (t / C::VSTAGES) & 1, prm.status,
-                            100000000ull);
-      }
+      // every load this thread issued has landed before the CTA exits (after
+      // an abort some were never awaited); each phase waited for is the last
+      // of its barrier, so on the normal path these return at once
+      mbar_wait_bounded(q_full, 0, prm.status, 100000000ull);
+      for (int t = max(0, kg_issued - C::STAGES); t < kg_issued; ++t)
+        mbar_wait_bounded(kg_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+                          100000000ull);
+      for (int t = max(0, v_issued - C::VSTAGES); t < v_issued; ++t)
+        mbar_wait_bounded(v_full + (t % C::VSTAGES), (t / C::VSTAGES) & 1, prm.status,
+                          100000000ull);
     }
   } else if (warp == kMmaWarp) {
     {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);    // gQ K^T: M=128 N=64
       constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // Q [K;gK]^T: N=128
       constexpr uint32_t id_w = idesc_bf16(128, D, false, true);    // W: N=D, B MN-major
-      bool ok = warp_wait(q_tmem, 0, abort_flag, prm.status);
+      bool ok = warp_wait(q_tmem, 0, abort_st, prm.status);
       const uint32_t tw = tmem + C::T_W, tq = tmem + C::T_QA, tgq = tmem + C::T_GQA;
       // S and G of tile t into buffer t & 1
       // waits and issue are split so that one tile's waits all come before
       // its MMAs: a wait right after a burst of MMA issue costs hundreds of
       // cycles even on a completed barrier
       auto wait_sg = [&](int t) -> bool {
-        return warp_wait(kg_full + t % C::STAGES, (t / C::STAGES) & 1, abort_flag, prm.status);
+        return warp_wait(kg_full + t % C::STAGES, (t / C::STAGES) & 1, abort_st, prm.status);
       };
       auto wait_w = [&](int t) -> bool {
-        return warp_wait(p_full + (t & 1), (t >> 1) & 1, abort_flag, prm.status) &&
-               warp_wait(v_full + t % C::VSTAGES, (t / C::VSTAGES) & 1, abort_flag, prm.status);
+        return warp_wait(p_full + (t & 1), (t >> 1) & 1, abort_st, prm.status) &&
+               warp_wait(v_full + t % C::VSTAGES, (t / C::VSTAGES) & 1, abort_st, prm.status);
       };
       auto issue_sg = [&](int t) {
         const int s = t % C::STAGES, b = t & 1;
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const bool has_g = has_gq || has_gk;
     f2 r_acc = {0.f, 0.f};  // even and odd keys summed apart
-    bool ok = warp_wait(q_full, 0, abort_flag, prm.status);
+    bool ok = warp_wait(q_full, 0, abort_st, prm.status);
     if (ok) {
       // stationary Q and gQ rows -> TMEM (bf16 pairs, lower half = even
       // feature): one 64-feature half-row per thread and tensor
@@ -371,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = t & 1;
       // buffer b last held tile t - 2, whose W MMAs completed before the S/G
       // MMAs of tile t (issued after them) signalled sg_full
-      if (!warp_wait(sg_full + b, (t >> 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+      if (!warp_wait(sg_full + b, (t >> 1) & 1, abort_st, prm.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[32], gr[32];
       const uint32_t ts = tmem + lane_off + C::T_S(b) + 32 * half,
@@ -412,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: r, D, sigma, graddO = W - r O ----
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) ok = warp_wait(w_done, 0, abort_flag, prm.status);
+    if (ok) ok = warp_wait(w_done, 0, abort_st, prm.status);
     tc_fence_after();
     part[half * 128 + row] = r_acc.x + r_acc.y;
     consumer_sync();
@@ -529,20 +533,28 @@ struct ColParams {
   __nv_bfloat16* gradv;
   float* acc;  // fp32 [B,H,N,D] gradQ accumulator
   int* status;
+  unsigned long long wait_ns;  // limit of one bounded wait
   int N, causal;
+  int BH, G;  // batch * heads, heads per CTA group (cta_coord)
   float scale;
   int has_gq, has_gk, has_gv;  // as in RowParams
 };
 
 // Pass 2 warp roles: warps 0-15 elementwise (warp w: TMEM lane quadrant w%4,
 // 16-column slice w/4 of the 64-query tile, which is also the 16-query
-// contraction step w/4 of the gradK / gradV MMAs), warp 16 TMA producer,
-// warp 17 TMEM allocator and MMA issuer.
+// contraction step w/4 of the gradK / gradV MMAs), warp 16 TMA producer of
+// the stationary tiles, the [Q|gQ] stages and the row scalars, warp 17 TMEM
+// allocator and MMA issuer, warp 18 TMA producer of the dO ring.  dO has a
+// warp of its own so that its loads run as far ahead as its ring allows:
+// the next tile's dP^T / H^T MMAs wait for it while the elementwise phase
+// runs, and the [Q|gQ] producer spends most of each tile waiting for the
+// gradK MMAs to free its stage.
 constexpr int kColConsumerWarps = 16;
 constexpr int kColConsumers = kColConsumerWarps * 32;
 constexpr int kColProducerWarp = kColConsumerWarps;
 constexpr int kColMmaWarp = kColConsumerWarps + 1;
-constexpr int kColThreads = (kColConsumerWarps + 2) * 32;
+constexpr int kColDoWarp = kColConsumerWarps + 2;
+constexpr int kColThreads = (kColConsumerWarps + 3) * 32;
 constexpr int kColCols = 64 / (kColConsumerWarps / 4);  // columns per elementwise thread
 static_assert(kColCols == 16, "one 16-query MMA step per column slice");
 
@@ -579,16 +591,17 @@ __global__ void __launch_bounds__(kColThreads, 1)
   static_assert((8 + 2 * C::STAGES + 2 * C::DSTAGES) * 8 <= 256,
                 "barriers end below the TMEM slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
+  Abort* abort_st = reinterpret_cast<Abort*>(smem + C::OFF_MISC + 264);
   float* scal = reinterpret_cast<float*>(smem + C::OFF_SC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = prm.N;
-  const int bh = blockIdx.y;
-  const int j0 = (int)blockIdx.x * C::BM;  // low key blocks (most query tiles) first
+  const CtaCoord cc = cta_coord(prm.BH, prm.G, (prm.N + C::BM - 1) / C::BM);
+  const int bh = cc.bh;
+  const int j0 = cc.blk * C::BM;  // low key blocks (most query tiles) first
   const int qstart = prm.causal ? (j0 / C::BN) * C::BN : 0;
   const int T = (N - qstart + C::BN - 1) / C::BN;
-  const int rot = (int)blockIdx.x % T;  // start tile of this CTA's query loop
+  const int rot = cc.blk % T;  // start tile of this CTA's query loop
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -607,7 +620,8 @@ __global__ void __launch_bounds__(kColThreads, 1)
     mbar_init(gq_empty, kColConsumers);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    abort_st->flag = 0;
+    abort_st->limit_ns = prm.wait_ns;
     fence_mbar_init();
   }
   if (warp == kColMmaWarp) {
@@ -645,9 +659,9 @@ __global__ void __launch_bounds__(kColThreads, 1)
       }
     };
     fetch(qstart + rotated(0, rot, T) * C::BN);
-    int qg_issued = 0, do_issued = 0;
+    int qg_issued = 0;
     for (int t = 0; t < T; ++t) {
-      const int s = t % C::STAGES, ds = t % C::DSTAGES;
+      const int s = t % C::STAGES;
       const int q0 = qstart + rotated(t, rot, T) * C::BN;
       const int q_next = qstart + rotated(t + 1 < T ? t + 1 : 0, rot, T) * C::BN;
       // Row scalars of tile t, stored negated (every one of them is
@@ -660,19 +674,11 @@ __global__ void __launch_bounds__(kColThreads, 1)
 #pragma unroll
         for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = -pre[a][u];
       __syncwarp();
-      // dO first: its ring is deeper, so it runs ahead of [Q|gQ]
+      // the next tile's scalars are in flight while this warp waits below
+      if (t + 1 < T) fetch(q_next);
       bool w = true;
-      if (lane == 0) {
-        if (t >= C::DSTAGES)
-          w = wait_bar(do_empty + ds, ((t / C::DSTAGES) - 1) & 1, abort_flag, prm.status);
-        if (w) {
-          mbar_arrive_expect_tx(do_full + ds, C::QB);
-          load_tile(smem + C::OFF_DO + ds * C::QB, &mDO, do_full + ds, q0, bh);
-          ++do_issued;
-        }
-        if (w && t >= C::STAGES)
-          w = wait_bar(qg_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status);
-      }
+      if (lane == 0 && t >= C::STAGES)
+        w = wait_bar(qg_empty + s, ((t / C::STAGES) - 1) & 1, abort_st, prm.status);
       ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       if (!ok) break;
       if (lane == 0) {
@@ -684,21 +690,37 @@ __global__ void __launch_bounds__(kColThreads, 1)
         if (t + 1 < T) {  // warm L2 with the next query tile
           tma_prefetch_l2_4d(&mQ, 0, q_next, 0, bh);
           if (has_gq) tma_prefetch_l2_4d(&mGQ, 0, q_next, 0, bh);
-          tma_prefetch_l2_4d(&mDO, 0, q_next, 0, bh);
         }
       }
-      if (t + 1 < T) fetch(q_next);
     }
+    // every load this warp issued has landed before the CTA exits (after an
+    // abort some were never awaited); each phase waited for is the last of
+    // its barrier, so on the normal path these return at once
     if (lane == 0) {
-      wait_bar(kv_full, 0, abort_flag, prm.status);
-      if (*abort_flag) {
-        for (int t = max(0, qg_issued - C::STAGES); t < qg_issued; ++t)
-          mbar_wait_bounded(qg_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
-                            100000000ull);
-        for (int t = max(0, do_issued - C::DSTAGES); t < do_issued; ++t)
-          mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
-                            100000000ull);
+      mbar_wait_bounded(kv_full, 0, prm.status, 100000000ull);
+      for (int t = max(0, qg_issued - C::STAGES); t < qg_issued; ++t)
+        mbar_wait_bounded(qg_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+                          100000000ull);
+    }
+  } else if (warp == kColDoWarp) {
+    if (lane == 0) {
+      int do_issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int ds = t % C::DSTAGES;
+        if (t >= C::DSTAGES &&
+            !wait_bar(do_empty + ds, ((t / C::DSTAGES) - 1) & 1, abort_st, prm.status))
+          break;
+        mbar_arrive_expect_tx(do_full + ds, C::QB);
+        load_tile(smem + C::OFF_DO + ds * C::QB, &mDO, do_full + ds,
+                  qstart + rotated(t, rot, T) * C::BN, bh);
+        ++do_issued;
+        if (t + 1 < T)  // warm L2 with the next dO tile
+          tma_prefetch_l2_4d(&mDO, 0, qstart + rotated(t + 1, rot, T) * C::BN, 0, bh);
       }
+      // every load this thread issued has landed before the CTA exits
+      for (int t = max(0, do_issued - C::DSTAGES); t < do_issued; ++t)
+        mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
+                          100000000ull);
     }
   } else if (warp == kColMmaWarp) {
     {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
@@ -722,7 +744,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
         const int ds = t % C::DSTAGES;
         const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
         const uint32_t v_l = opaque(v_lo), gv_l = opaque(gv_lo);
-        if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_flag, prm.status)) return false;
+        if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_st, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
@@ -742,8 +764,8 @@ __global__ void __launch_bounds__(kColThreads, 1)
         const int s = t % C::STAGES;
         const uint32_t qgq_lo = opaque(lo_kmajor(sb + C::OFF_QG + s * 2 * C::QB));  // [Q;gQ] per half
         const uint32_t k_l = opaque(k_lo), gk_l = opaque(gk_lo);
-        if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
-        if (C::GQ_IN_S && t >= 1 && !warp_wait(gq_empty, (t - 1) & 1, abort_flag, prm.status))
+        if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_st, prm.status)) return false;
+        if (C::GQ_IN_S && t >= 1 && !warp_wait(gq_empty, (t - 1) & 1, abort_st, prm.status))
           return false;
         tc_fence_after();
         // [S^T | K gQ^T] = K [Q; gQ]^T (S^T = K Q^T alone without gQ), then
@@ -763,17 +785,17 @@ __global__ void __launch_bounds__(kColThreads, 1)
         mma_commit_w(sc_full);
         return true;
       };
-      bool ok = warp_wait(kv_full, 0, abort_flag, prm.status) && issue_dh(0) && issue_sg(0);
+      bool ok = warp_wait(kv_full, 0, abort_st, prm.status) && issue_dh(0) && issue_sg(0);
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES, ds = t % C::DSTAGES;
         // ---- next tile's dP^T, H^T while the elementwise warps work ----
         if (C::EARLY_DH && t + 1 < T) {
-          if (!warp_wait(sc_read, t & 1, abort_flag, prm.status)) { ok = false; break; }
+          if (!warp_wait(sc_read, t & 1, abort_st, prm.status)) { ok = false; break; }
           tc_fence_after();
           if (!issue_dh(t + 1)) { ok = false; break; }
         }
         // ---- outputs: A operands (bf16 gS^T, dS^T, gdP^T) from TMEM ----
-        if (!warp_wait(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (!warp_wait(ds_full, t & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t qgq_s = sb + C::OFF_QG + s * 2 * C::QB;
         // B operands MN-major: 64-feature groups 2*BN*128 bytes apart in the
@@ -794,7 +816,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
         // read first (MMAs from one thread run in issue order)
         auto issue_gq = [&]() -> bool {
           if (!C::GQ_IN_S && t >= 1) {
-            if (!warp_wait(gq_empty, (t - 1) & 1, abort_flag, prm.status)) return false;
+            if (!warp_wait(gq_empty, (t - 1) & 1, abort_st, prm.status)) return false;
             tc_fence_after();
           }
           const uint32_t k_m = opaque(k_mn), gk_m = opaque(gk_mn), ds_m = opaque(ds_mn),
@@ -844,18 +866,13 @@ __global__ void __launch_bounds__(kColThreads, 1)
     auto reduce_gq = [&](int t, const uint32_t (&gq)[NC]) {
       const int qa = qstart + rotated(t, rot, T) * C::BN + NC * slice;
       if (D == 128) {
-        float* base = prm.acc + ((size_t)bh * N + qa) * D + row;
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-          if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
+        red_columns<NC>(prm.acc + ((size_t)bh * N + qa) * D + row, D, gq, N - qa);
       } else {
         // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
         // lanes 32w' + x; the upper 16 lanes of each warp hold nothing.
         if (lane < 16) {
-          float* base = prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane;
-#pragma unroll
-          for (int c = 0; c < NC; ++c)
-            if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(gq[c]) * prm.scale);
+          red_columns<NC>(prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane, D, gq,
+                          N - qa);
         }
       }
     };
@@ -863,9 +880,9 @@ __global__ void __launch_bounds__(kColThreads, 1)
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
       const int q0 = qstart + rotated(t, rot, T) * C::BN;
-      if (!warp_wait(sc_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+      if (!warp_wait(sc_full, t & 1, abort_st, prm.status)) { ok = false; break; }
       // the stage's row scalars were published with qg_full (already complete)
-      if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+      if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_st, prm.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[NC], dpr[NC], gr[NC], hr[NC];
       const uint32_t tl = tmem + lane_off + NC * slice;
@@ -927,7 +944,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
       // With LATE_GQ the previous tile's gradQ^T MMAs read the dS^T / gS^T
       // tiles below: wait for them first (their result stays in TMEM until
       // gq_empty).  Otherwise that wait ended the previous iteration.
-      if (C::LATE_GQ && t >= 1 && !warp_wait(gq_full, (t - 1) & 1, abort_flag, prm.status)) {
+      if (C::LATE_GQ && t >= 1 && !warp_wait(gq_full, (t - 1) & 1, abort_st, prm.status)) {
         ok = false;
         break;
       }
@@ -951,13 +968,13 @@ __global__ void __launch_bounds__(kColThreads, 1)
           reduce_gq(t - 1, gq);
         }
       } else {
-        if (!warp_wait(gq_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (!warp_wait(gq_full, t & 1, abort_st, prm.status)) { ok = false; break; }
         load_gq(gq);
         reduce_gq(t, gq);
       }
     }
     if (C::LATE_GQ && ok && T >= 1) {
-      ok = warp_wait(gq_full, (T - 1) & 1, abort_flag, prm.status);
+      ok = warp_wait(gq_full, (T - 1) & 1, abort_st, prm.status);
       if (ok) {
         uint32_t gq[NC];
         load_gq(gq);
@@ -966,7 +983,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
     }
     // ---- epilogue: gradK (scaled), gradV; each thread D/4 features ----
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) ok = warp_wait(acc_done, 0, abort_flag, prm.status);
+    if (ok) ok = warp_wait(acc_done, 0, abort_st, prm.status);
     tc_fence_after();
     if (ok) {  // warp-uniform: every lane loads TMEM, rows past N do not store
       constexpr int PART = D / 4;
@@ -1003,14 +1020,15 @@ __global__ void __launch_bounds__(kColThreads, 1)
   }
 }
 
-// fp32 accumulator -> bf16, 8 elements per thread.
+// scale * fp32 accumulator -> bf16, 8 elements per thread.
 __global__ void __launch_bounds__(256) gradq_convert(const float4* __restrict__ acc,
-                                                     uint4* __restrict__ out, size_t n8) {
+                                                     uint4* __restrict__ out, size_t n8,
+                                                     float scale) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
        i += (size_t)gridDim.x * blockDim.x) {
     const float4 a = acc[2 * i], b = acc[2 * i + 1];
-    out[i] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y),
-                        pack_bf16(b.z, b.w));
+    out[i] = make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
+                        pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
   }
 }
 
@@ -1059,13 +1077,16 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
   rp.D_out = ws.D;
   rp.acc_zero = ws.acc;
   rp.status = ws.status;
+  rp.wait_ns = wait_limit_ns();
   rp.N = p.N;
+  rp.BH = p.BH();
+  rp.G = cta_group_heads(p.BH(), (p.N + R::BM - 1) / R::BM, sm_count());
   rp.causal = p.causal;
   rp.scale = p.scale;
   rp.has_gq = has_gq;
   rp.has_gk = has_gk;
   rp.has_gv = has_gv;
-  dim3 g1((p.N + R::BM - 1) / R::BM, p.BH());
+  dim3 g1((unsigned)(((p.N + R::BM - 1) / R::BM) * p.BH()));
   row_kernel<<<g1, kThreads, R::SMEM, log.stream>>>(mQr, mGQr, mKr, mGKr, mVr, mGVr, rp);
   e = cudaGetLastError();
   log.mark();
@@ -1080,19 +1101,22 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
   cp.gradv = static_cast<__nv_bfloat16*>(gradv);
   cp.acc = ws.acc;
   cp.status = ws.status;
+  cp.wait_ns = wait_limit_ns();
   cp.N = p.N;
+  cp.BH = p.BH();
+  cp.G = cta_group_heads(p.BH(), (p.N + Cc::BM - 1) / Cc::BM, sm_count());
   cp.causal = p.causal;
   cp.scale = p.scale;
   cp.has_gq = has_gq;
   cp.has_gk = has_gk;
   cp.has_gv = has_gv;
-  dim3 g2((p.N + Cc::BM - 1) / Cc::BM, p.BH());
+  dim3 g2((unsigned)(((p.N + Cc::BM - 1) / Cc::BM) * p.BH()));
   col_kernel<<<g2, kColThreads, Cc::SMEM, log.stream>>>(mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc, cp);
   e = cudaGetLastError();
   log.mark();
   if (e != cudaSuccess) return e;
 
-  return launch_acc_to_bf16(ws.acc, gradq, p.elems(), log);
+  return launch_acc_to_bf16(ws.acc, gradq, p.elems(), p.scale, log);
 }
 
 // One thread waits on an mbarrier whose phase nothing completes; the bounded
@@ -1117,11 +1141,12 @@ cudaError_t launch_wait_timeout_selftest(int* status, long long limit_ns, cudaSt
 
 bool tc_supported(const Problem& p) { return p.bf16 && (p.d == 64 || p.d == 128); }
 
-cudaError_t launch_acc_to_bf16(const float* acc, void* out, size_t elems, LaunchLog& log) {
+cudaError_t launch_acc_to_bf16(const float* acc, void* out, size_t elems, float scale,
+                               LaunchLog& log) {
   const size_t n8 = elems / 8;
   const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 152 * 16);
   gradq_convert<<<blocks, 256, 0, log.stream>>>(reinterpret_cast<const float4*>(acc),
-                                                static_cast<uint4*>(out), n8);
+                                                static_cast<uint4*>(out), n8, scale);
   const cudaError_t e = cudaGetLastError();
   log.mark();
   return e;

@@ -89,7 +89,9 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int* status;
+  unsigned long long wait_ns;  // limit of one bounded wait
   int N, causal;
+  int BH, G;  // batch * heads, heads per CTA group (cta_coord)
   float scale;
 };
 
@@ -120,15 +122,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   static_assert((12 + 2 * C::KSTAGES + 2 * C::VSTAGES) * 8 <= 256,
                 "barriers end below the TMEM slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
+  Abort* abort_st = reinterpret_cast<Abort*>(smem + C::OFF_MISC + 264);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = prm.N;
-  const int bh = blockIdx.y;
+  const int nblk = (prm.N + C::BM - 1) / C::BM;
+  const CtaCoord cc = cta_coord(prm.BH, prm.G, nblk);
+  const int bh = cc.bh;
   // heavy (late) row blocks first under a causal mask
-  const int nblk = gridDim.x;
-  const int blk = prm.causal ? (nblk - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const int blk = prm.causal ? (nblk - 1 - cc.blk) : cc.blk;
   const int i0 = blk * C::BM;
   const int kend = prm.causal ? min(N, i0 + C::BM) : N;
   const int T = (kend + C::BN - 1) / C::BN;
@@ -154,7 +157,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(red_full + 1, kFwdConsumers);
     mbar_init(q_tmem, kFwdConsumers);
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    abort_st->flag = 0;
+    abort_st->limit_ns = prm.wait_ns;
     fence_mbar_init();
   }
   if (warp == kFwdMmaWarp) {
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       auto load_k = [&](int t) -> bool {
         const int s = t % C::KSTAGES;
         if (t >= C::KSTAGES &&
-            !wait_bar(k_empty + s, ((t / C::KSTAGES) - 1) & 1, abort_flag, prm.status))
+            !wait_bar(k_empty + s, ((t / C::KSTAGES) - 1) & 1, abort_st, prm.status))
           return false;
         mbar_arrive_expect_tx(k_full + s, C::KB);
         load_tile(smem + C::OFF_K + s * C::KB, &mK, k_full + s, rotated(t, rot, T) * C::BN, bh);
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       auto load_v = [&](int t) -> bool {
         const int s = t % C::VSTAGES;
         if (t >= C::VSTAGES &&
-            !wait_bar(v_empty + s, ((t / C::VSTAGES) - 1) & 1, abort_flag, prm.status))
+            !wait_bar(v_empty + s, ((t / C::VSTAGES) - 1) & 1, abort_st, prm.status))
           return false;
         mbar_arrive_expect_tx(v_full + s, C::KB);
         load_tile(smem + C::OFF_V + s * C::KB, &mV, v_full + s, rotated(t, rot, T) * C::BN, bh);
@@ -197,29 +201,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (t + 1 < T && !load_k(t + 1)) break;
         if (!load_v(t)) break;
       }
-      // after an abort, loads still in flight must land before the CTA exits
-      if (*abort_flag) {
-        mbar_wait_bounded(q_full, 0, prm.status, 100000000ull);
-        for (int t = max(0, k_issued - C::KSTAGES); t < k_issued; ++t)
-          mbar_wait_bounded(k_full + (t % C::KSTAGES), (t / C::KSTAGES) & 1, prm.status,
-                            100000000ull);
-        for (int t = max(0, v_issued - C::VSTAGES); t < v_issued; ++t)
-          mbar_wait_bounded(v_full + (t % C::VSTAGES), (t / C::VSTAGES) & 1, prm.status,
-                            100000000ull);
-      }
+      // every load this thread issued has landed before the CTA exits (after
+      // an abort some were never awaited); each phase waited for is the last
+      // of its barrier, so on the normal path these return at once
+      mbar_wait_bounded(q_full, 0, prm.status, 100000000ull);
+      for (int t = max(0, k_issued - C::KSTAGES); t < k_issued; ++t)
+        mbar_wait_bounded(k_full + (t % C::KSTAGES), (t / C::KSTAGES) & 1, prm.status,
+                          100000000ull);
+      for (int t = max(0, v_issued - C::VSTAGES); t < v_issued; ++t)
+        mbar_wait_bounded(v_full + (t % C::VSTAGES), (t / C::VSTAGES) & 1, prm.status,
+                          100000000ull);
     }
   } else if (warp == kFwdMmaWarp) {
     {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
       constexpr uint32_t id_s = idesc_bf16(128, C::BN, false, false);  // S = Q K^T: N = BN
       constexpr uint32_t id_o = idesc_bf16(128, D, false, true);       // O += P V: N = D, B MN
       const uint32_t t_o = tmem + C::T_O, t_q = tmem + C::T_QA;
-      bool ok = warp_wait(q_tmem, 0, abort_flag, prm.status);
+      bool ok = warp_wait(q_tmem, 0, abort_st, prm.status);
       // O += P(t) V(t), A = bf16 P from TMEM (in S buffer t & 1), contraction
       // over the tile's keys; o_ready completes once per tile
       auto issue_pv = [&](int t) -> bool {
         const int pb = t & 1, vs = t % C::VSTAGES;
-        if (!warp_wait(p_full + pb, (t >> 1) & 1, abort_flag, prm.status)) return false;
-        if (!warp_wait(v_full + vs, (t / C::VSTAGES) & 1, abort_flag, prm.status)) return false;
+        if (!warp_wait(p_full + pb, (t >> 1) & 1, abort_st, prm.status)) return false;
+        if (!warp_wait(v_full + vs, (t / C::VSTAGES) & 1, abort_st, prm.status)) return false;
         tc_fence_after();
         const uint32_t v_mn = opaque(lo_mnmajor(sb + C::OFF_V + vs * C::KB, C::BN * 128));
         const uint32_t t_p = tmem + C::T_S(pb);
@@ -234,8 +238,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // consumed by the P V MMAs of tile t - 2, issued before S(t)
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::KSTAGES, b = t & 1;
-        if (!warp_wait(k_full + s, (t / C::KSTAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
-        if (t >= 2 && !warp_wait(s_empty + b, ((t >> 1) - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (!warp_wait(k_full + s, (t / C::KSTAGES) & 1, abort_st, prm.status)) { ok = false; break; }
+        if (t >= 2 && !warp_wait(s_empty + b, ((t >> 1) - 1) & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_lo = opaque(lo_kmajor(sb + C::OFF_K + s * C::KB));
         const uint32_t t_s = tmem + C::T_S(b);
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const float sc2 = prm.scale * kLog2e;
     const f2 sc2_2 = {sc2, sc2};
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    bool ok = warp_wait(q_full, 0, abort_flag, prm.status);
+    bool ok = warp_wait(q_full, 0, abort_st, prm.status);
     if (ok) {
       // stationary Q row -> TMEM (bf16 pairs, lower half = even feature): one
       // 64-feature half-row per thread of slices 0 .. D/64 - 1
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     float m = -INFINITY, l = 0.f;
     for (int t = 0; ok && t < T; ++t) {
       const int b = t & 1;
-      if (!warp_wait(s_full + b, (t >> 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+      if (!warp_wait(s_full + b, (t >> 1) & 1, abort_st, prm.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[NC];
       tmem_ld32(tmem + lane_off + C::T_S(b) + NC * slice, sr);
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       float* rt = red + b * NS * 128;
       rt[slice * 128 + row] = mx * sc2;
       mbar_arrive(red_full + b);
-      if (!warp_wait(red_full + b, (t >> 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+      if (!warp_wait(red_full + b, (t >> 1) & 1, abort_st, prm.status)) { ok = false; break; }
       float mt = -INFINITY;
 #pragma unroll
       for (int u = 0; u < NS; ++u) mt = fmaxf(mt, rt[u * 128 + row]);
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // branch when any lane needs it; the other lanes scale by 1.
       const bool scale_o = move && t >= 1 && m > -INFINITY;
       if (__any_sync(0xffffffffu, scale_o)) {
-        if (!warp_wait(o_ready, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (!warp_wait(o_ready, (t - 1) & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
         const float f = scale_o ? alpha : 1.f;
         constexpr int PART = D / NS;
@@ -380,7 +384,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
     for (int u = 0; u < NS; ++u) L += part[u * 128 + row];
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) ok = warp_wait(o_ready, (T - 1) & 1, abort_flag, prm.status);
+    if (ok) ok = warp_wait(o_ready, (T - 1) & 1, abort_st, prm.status);
     tc_fence_after();
     if (ok) {
       const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -447,7 +451,9 @@ struct BwdParams {
   __nv_bfloat16* dv;
   float* acc;  // fp32 [B,H,N,D] dQ accumulator
   int* status;
+  unsigned long long wait_ns;  // limit of one bounded wait
   int N, causal;
+  int BH, G;  // batch * heads, heads per CTA group (cta_coord)
   float scale;
 };
 
@@ -484,16 +490,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* acc_done = dq_empty + 1;
   uint64_t* drain = acc_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
+  Abort* abort_st = reinterpret_cast<Abort*>(smem + C::OFF_MISC + 264);
   float* scal = reinterpret_cast<float*>(smem + C::OFF_SC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = prm.N;
-  const int bh = blockIdx.y;
-  const int j0 = (int)blockIdx.x * C::BM;
+  const CtaCoord cc = cta_coord(prm.BH, prm.G, (prm.N + C::BM - 1) / C::BM);
+  const int bh = cc.bh;
+  const int j0 = cc.blk * C::BM;
   const int qstart = prm.causal ? (j0 / C::BN) * C::BN : 0;
   const int T = (N - qstart + C::BN - 1) / C::BN;
-  const int rot = (int)blockIdx.x % T;
+  const int rot = cc.blk % T;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -512,7 +519,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(dq_empty, kBwdConsumers);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    abort_st->flag = 0;
+    abort_st->limit_ns = prm.wait_ns;
     fence_mbar_init();
   }
   if (warp == kBwdMmaWarp) {
@@ -552,14 +560,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool w = true;
       if (lane == 0) {
         if (t >= C::DSTAGES)
-          w = wait_bar(do_empty + ds, ((t / C::DSTAGES) - 1) & 1, abort_flag, prm.status);
+          w = wait_bar(do_empty + ds, ((t / C::DSTAGES) - 1) & 1, abort_st, prm.status);
         if (w) {
           mbar_arrive_expect_tx(do_full + ds, C::QB);
           load_tile(smem + C::OFF_DO + ds * C::QB, &mDO, do_full + ds, q0, bh);
           ++do_issued;
         }
         if (w && t >= C::STAGES)
-          w = wait_bar(q_empty + s, ((t / C::STAGES) - 1) & 1, abort_flag, prm.status);
+          w = wait_bar(q_empty + s, ((t / C::STAGES) - 1) & 1, abort_st, prm.status);
       }
       if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) break;
       // the stage's scalars were last read by the elementwise warps of tile
@@ -578,16 +586,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (t + 1 < T) fetch(qstart + rotated(t + 1, rot, T) * C::BN);
     }
+    // every load this warp issued has landed before the CTA exits (after an
+    // abort some were never awaited); each phase waited for is the last of
+    // its barrier, so on the normal path these return at once
     if (lane == 0) {
-      wait_bar(kv_full, 0, abort_flag, prm.status);
-      if (*abort_flag) {
-        for (int t = max(0, q_issued - C::STAGES); t < q_issued; ++t)
-          mbar_wait_bounded(q_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
-                            100000000ull);
-        for (int t = max(0, do_issued - C::DSTAGES); t < do_issued; ++t)
-          mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
-                            100000000ull);
-      }
+      mbar_wait_bounded(kv_full, 0, prm.status, 100000000ull);
+      for (int t = max(0, q_issued - C::STAGES); t < q_issued; ++t)
+        mbar_wait_bounded(q_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+                          100000000ull);
+      for (int t = max(0, do_issued - C::DSTAGES); t < do_issued; ++t)
+        mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
+                          100000000ull);
     }
   } else if (warp == kBwdMmaWarp) {
     {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
@@ -604,7 +613,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int ds = t % C::DSTAGES;
         const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
         const uint32_t v_l = opaque(v_lo);
-        if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_flag, prm.status)) return false;
+        if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_st, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
@@ -618,7 +627,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int s = t % C::STAGES;
         const uint32_t q_lo = opaque(lo_kmajor(sb + C::OFF_Q + s * C::QB));
         const uint32_t k_l = opaque(k_lo);
-        if (!warp_wait(q_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) return false;
+        if (!warp_wait(q_full + s, (t / C::STAGES) & 1, abort_st, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
@@ -627,15 +636,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit_w(sc_full);
         return true;
       };
-      bool ok = warp_wait(kv_full, 0, abort_flag, prm.status) && issue_dp(0) && issue_s(0);
+      bool ok = warp_wait(kv_full, 0, abort_st, prm.status) && issue_dp(0) && issue_s(0);
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES, ds = t % C::DSTAGES;
         if (C::EARLY_DP && t + 1 < T) {
-          if (!warp_wait(sc_read, t & 1, abort_flag, prm.status)) { ok = false; break; }
+          if (!warp_wait(sc_read, t & 1, abort_st, prm.status)) { ok = false; break; }
           tc_fence_after();
           if (!issue_dp(t + 1)) { ok = false; break; }
         }
-        if (!warp_wait(ds_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
+        if (!warp_wait(ds_full, t & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
         {
           const uint32_t q_mn = opaque(lo_mnmajor(sb + C::OFF_Q + s * C::QB, C::BN * 128));
@@ -657,7 +666,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!C::EARLY_DP && t + 1 < T && !issue_dp(t + 1)) { ok = false; break; }
         if (t + 1 < T && !issue_s(t + 1)) { ok = false; break; }
         if (t >= 1) {
-          if (!warp_wait(dq_empty, (t - 1) & 1, abort_flag, prm.status)) { ok = false; break; }
+          if (!warp_wait(dq_empty, (t - 1) & 1, abort_st, prm.status)) { ok = false; break; }
           tc_fence_after();
         }
         {
@@ -684,7 +693,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // dQ^T partial of a finished tile (TMEM lane = feature index, column =
     // query) into the fp32 accumulator
     auto drain_dq = [&](int t, uint32_t (&dq)[NC]) -> bool {
-      if (!warp_wait(dq_full, t & 1, abort_flag, prm.status)) return false;
+      if (!warp_wait(dq_full, t & 1, abort_st, prm.status)) return false;
       tc_fence_after();
       tmem_ld16(tmem + lane_off + C::T_DQ + NC * slice, dq);
       tc_fence_before();
@@ -694,18 +703,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto reduce_dq = [&](int t, const uint32_t (&dq)[NC]) {
       const int qa = qstart + rotated(t, rot, T) * C::BN + NC * slice;
       if (D == 128) {
-        float* base = prm.acc + ((size_t)bh * N + qa) * D + row;
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-          if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(dq[c]) * prm.scale);
+        red_columns<NC>(prm.acc + ((size_t)bh * N + qa) * D + row, D, dq, N - qa);
       } else {
         // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
         // lanes 32w' + x; the upper 16 lanes of each warp hold nothing
         if (lane < 16) {
-          float* base = prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane;
-#pragma unroll
-          for (int c = 0; c < NC; ++c)
-            if (qa + c < N) atomicAdd(base + (size_t)c * D, __uint_as_float(dq[c]) * prm.scale);
+          red_columns<NC>(prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane, D, dq,
+                          N - qa);
         }
       }
     };
@@ -713,8 +717,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
       const int q0 = qstart + rotated(t, rot, T) * C::BN;
-      if (!warp_wait(sc_full, t & 1, abort_flag, prm.status)) { ok = false; break; }
-      if (!warp_wait(q_full + s, (t / C::STAGES) & 1, abort_flag, prm.status)) { ok = false; break; }
+      if (!warp_wait(sc_full, t & 1, abort_st, prm.status)) { ok = false; break; }
+      if (!warp_wait(q_full + s, (t / C::STAGES) & 1, abort_st, prm.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[NC], dpr[NC];
       const uint32_t tl = tmem + lane_off + NC * slice;
@@ -781,7 +785,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     // ---- epilogue: dK (scaled), dV; each thread D/4 features ----
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) ok = warp_wait(acc_done, 0, abort_flag, prm.status);
+    if (ok) ok = warp_wait(acc_done, 0, abort_st, prm.status);
     tc_fence_after();
     if (ok) {
       constexpr int PART = D / 4;
@@ -864,10 +868,13 @@ cudaError_t forward_d(const Problem& p, const void* q, const void* k, const void
   fp.o = static_cast<__nv_bfloat16*>(o);
   fp.lse = lse;
   fp.status = ws.status;
+  fp.wait_ns = wait_limit_ns();
   fp.N = p.N;
+  fp.BH = p.BH();
+  fp.G = cta_group_heads(p.BH(), (p.N + C::BM - 1) / C::BM, sm_count());
   fp.causal = p.causal;
   fp.scale = p.scale;
-  dim3 grid((p.N + C::BM - 1) / C::BM, p.BH());
+  dim3 grid((unsigned)(((p.N + C::BM - 1) / C::BM) * p.BH()));
   fwd_row_pass<D><<<grid, kFwdThreads, C::SMEM, log.stream>>>(mQ, mK, mV, fp);
   e = cudaGetLastError();
   log.mark();
@@ -902,15 +909,18 @@ cudaError_t backward_d(const Problem& p, const void* q, const void* k, const voi
   bp.dv = static_cast<__nv_bfloat16*>(dv);
   bp.acc = ws.acc;
   bp.status = ws.status;
+  bp.wait_ns = wait_limit_ns();
   bp.N = p.N;
+  bp.BH = p.BH();
+  bp.G = cta_group_heads(p.BH(), (p.N + C::BM - 1) / C::BM, sm_count());
   bp.causal = p.causal;
   bp.scale = p.scale;
-  dim3 grid((p.N + C::BM - 1) / C::BM, p.BH());
+  dim3 grid((unsigned)(((p.N + C::BM - 1) / C::BM) * p.BH()));
   bwd_col_pass<D><<<grid, kBwdThreads, C::SMEM, log.stream>>>(mK, mV, mQ, mDO, bp);
   e = cudaGetLastError();
   log.mark();
   if (e != cudaSuccess) return e;
-  return launch_acc_to_bf16(ws.acc, dq, p.elems(), log);
+  return launch_acc_to_bf16(ws.acc, dq, p.elems(), p.scale, log);
 }
 
 }  // namespace

@@ -22,29 +22,39 @@ constexpr float kLog2e = 1.4426950408889634f;
 // MN-major operand descriptor convention: LBO = stride between 64-element
 // groups along M/N, SBO = stride between 8-row groups along K.
 
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         int* status) {
+// Per-CTA abort state in shared memory: the flag that tells every role of
+// the CTA to stop, and the time limit of one bounded wait (a kernel argument,
+// written once before the CTA's first barrier).
+struct Abort {
+  volatile int flag;
+  int pad;
+  uint64_t limit_ns;
+};
+
+// Bounded wait that also gives up as soon as another role has aborted.  A
+// failed poll sleeps until the phase completes or 10 us pass (less for a
+// shorter limit); the abort flag and the time limit are checked after each.
+constexpr uint32_t kPollSleepNs = 10000;
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Abort* ab, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
-        report_status(status, FBOB_ERR_TIMEOUT);
-        *abort_flag = 1;
-        return false;
-      }
+  const uint64_t limit = ab->limit_ns;
+  const uint32_t sleep = limit < kPollSleepNs ? (uint32_t)limit : kPollSleepNs;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, sleep)) return true;
+    if (ab->flag) return false;
+    if (global_ns() - t0 > limit) {
+      report_status(status, FBOB_ERR_TIMEOUT);
+      ab->flag = 1;
+      return false;
     }
   }
 }
 
 // Warp-uniform bounded wait: tcgen05.ld is .sync.aligned, so every lane of
 // a warp must take the same branch after a wait.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
-  const bool ok = wait_bar(bar, parity, abort_flag, status);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Abort* ab, int* status) {
+  const bool ok = wait_bar(bar, parity, ab, status);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -52,6 +62,61 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 template <int THREADS>
 __device__ __forceinline__ void named_sync(int id) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(THREADS) : "memory");
+}
+
+// One-dimensional grid of nblk * BH CTAs.  Heads are taken in groups of G;
+// within a group the block index varies slowest, so block 0 of every head
+// of the group starts before block 1 of any.  With the heaviest block of a
+// head numbered 0, the long CTAs start first and short ones fill the tail,
+// while the CTAs that run at the same time belong to a few heads only, whose
+// streamed tiles stay in L2.  G is chosen on the host (cta_group_heads).
+struct CtaCoord {
+  int bh, blk;
+};
+__device__ __forceinline__ CtaCoord cta_coord(int BH, int G, int nblk) {
+  const int i = (int)blockIdx.x;
+  const int per_group = G * nblk;
+  const int g = i / per_group;
+  const int j = i - g * per_group;
+  const int gs = min(G, BH - g * G);  // heads in this (possibly last) group
+  return {g * G + j % gs, j / gs};
+}
+
+// Number of SMs of the current device (looked up once per process).
+inline int sm_count() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+  });
+  return n;
+}
+
+// Heads per group: enough that a group holds at least two waves of CTAs.
+inline int cta_group_heads(int BH, int nblk, int sms) {
+  int G = 1;
+  while (G < BH && (long long)G * nblk < 2ll * sms) G *= 2;
+  return G < BH ? G : BH;
+}
+
+// Adds this thread's NC fp32 partials (consecutive columns, `stride`
+// elements apart in the accumulator) with one global reduction each; only the
+// first `valid` are inside the sequence.  The scale factor of dQ / gradQ is
+// applied once, when the accumulator is converted to bf16.
+template <int NC>
+__device__ __forceinline__ void red_columns(float* base, size_t stride, const uint32_t (&v)[NC],
+                                            int valid) {
+  if (valid >= NC) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) atomicAdd(base + (size_t)c * stride, __uint_as_float(v[c]));
+  } else {
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      if (c < valid) atomicAdd(base + (size_t)c * stride, __uint_as_float(v[c]));
+  }
 }
 
 // Tile visited at step t when a CTA starts its loop at tile `rot` and wraps:

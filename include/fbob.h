@@ -188,6 +188,18 @@ int fbob_force_path(int path);
  * the hook off.  Returns FBOB_OK or FBOB_ERR_INVALID_ARG. */
 int fbob_set_profile_events(void* const* events, int count);
 
+/* Process-wide limit, in nanoseconds, of one device-side bounded wait in the
+ * tensor-core kernels (default 2 s, far above any legitimate wait).  A wait
+ * that runs out records FBOB_ERR_TIMEOUT in the call's status word; every
+ * role of that thread block then stops early, waits (with a fixed 100 ms
+ * limit of its own) for the copies and MMAs it has in flight, and exits, and
+ * the call's outputs are undefined.  The limit is checked each time the
+ * waiting thread wakes, at least every 10 us.  ns = 0 restores the default;
+ * 1 <= ns <= 6e10 sets it.
+ * Applies to calls enqueued afterwards.  Returns the previous limit, or -1
+ * (nothing changed) for a value out of range.  Not synchronised. */
+long long fbob_set_wait_limit(long long ns);
+
 /* Number of kernels the last enqueued call launched (for launch counting). */
 int fbob_last_launch_count(void);
 

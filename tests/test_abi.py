@@ -154,6 +154,15 @@ def test_profile_event_hook_validation(lib):
     assert lib.fbob_set_profile_events(None, 0) == 0
 
 
+def test_wait_limit_setting(lib):
+    old = lib.fbob_set_wait_limit(5000)        # 5 us
+    assert old == 2_000_000_000                 # the 2 s default
+    assert lib.fbob_set_wait_limit(-1) == -1    # out of range: unchanged
+    assert lib.fbob_set_wait_limit(61_000_000_000) == -1
+    assert lib.fbob_set_wait_limit(0) == 5000   # 0 restores the default
+    assert lib.fbob_set_wait_limit(0) == 2_000_000_000
+
+
 def test_selftest_rejects_bad_arguments(lib):
     assert lib.fbob_selftest_wait_timeout(None, 256, 10, None) == 1
     assert lib.fbob_selftest_wait_timeout(ctypes.c_void_p(1 << 20), 16, 10, None) == 1

@@ -88,6 +88,37 @@ def test_bounded_wait_times_out_and_context_survives():
     assert torch.isfinite(o.float()).all()
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_real_kernels_stop_cleanly_when_their_waits_run_out(d):
+    """fbob_bob with a 1 ns wait limit: the first wait of each thread block
+    that is not already complete runs out.  That block records
+    FBOB_ERR_TIMEOUT, every role of it stops, waits for its own copies and
+    MMAs in flight, frees its TMEM and exits; the call reports the timeout
+    through fbob_status, the GPU context stays usable, and the next call,
+    with the default limit, is correct."""
+    w = Workload("abort", 1, 2, 300, d, "bf16", True, 1.0, 1.0, 0.3)
+    ins = {k: v.cuda() for k, v in make_inputs(w, seed=13).items()}
+    args = (ins["q"], ins["k"], ins["v"])
+    o, lse = fbob.forward(*args, True, w.scale)
+    cot = (ins["do"], ins["gq"], ins["gk"], ins["gv"])
+    ws = fbob.alloc_workspace(fbob.OP_BOB, fbob.shape_of(ins["q"], True, w.scale), "cuda")
+    ref = fbob.bob(*args, o, lse, *cot, True, w.scale, workspace=ws)
+    assert fbob.status(ws) == 0
+    old = fbob.set_wait_limit(1)
+    try:
+        fbob.bob(*args, o, lse, *cot, True, w.scale, workspace=ws)
+        st = fbob.status(ws)
+    finally:
+        fbob.set_wait_limit(old)
+    assert st == 5  # FBOB_ERR_TIMEOUT
+    got = fbob.bob(*args, o, lse, *cot, True, w.scale, workspace=ws)
+    assert fbob.status(ws) == 0
+    torch.cuda.synchronize()
+    for g, r in zip(got, ref):
+        err = ((g.double() - r.double()).abs().max() / r.double().abs().max()).item()
+        assert err <= 1e-2, err
+
+
 def test_launch_count_is_reported():
     w = Workload("count", 1, 1, 128, 64, "bf16", True, 1.0, 1.0, 0.2)
     ins = {k: v.cuda() for k, v in make_inputs(w, seed=3).items()}
