@@ -260,15 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = warp_wait(q_tmem, 0, abort_st, prm.status);
       const uint32_t tw = tmem + C::T_W, tq = tmem + C::T_QA, tgq = tmem + C::T_GQA;
       // S and G of tile t into buffer t & 1
-      // waits and issue are split so that one tile's waits all come before
-      // its MMAs: a wait right after a burst of MMA issue costs hundreds of
-      // cycles even on a completed barrier
       auto wait_sg = [&](int t) -> bool {
         return warp_wait(kg_full + t % C::STAGES, (t / C::STAGES) & 1, abort_st, prm.status);
       };
-      auto wait_w = [&](int t) -> bool {
-        return warp_wait(p_full + (t & 1), (t >> 1) & 1, abort_st, prm.status) &&
-               warp_wait(v_full + t % C::VSTAGES, (t / C::VSTAGES) & 1, abort_st, prm.status);
+      auto wait_p = [&](int t) -> bool {
+        return warp_wait(p_full + (t & 1), (t >> 1) & 1, abort_st, prm.status);
+      };
+      auto wait_v = [&](int t) -> bool {
+        return warp_wait(v_full + t % C::VSTAGES, (t / C::VSTAGES) & 1, abort_st, prm.status);
       };
       auto issue_sg = [&](int t) {
         const int s = t % C::STAGES, b = t & 1;
@@ -319,12 +318,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_sg(t);
         }
       }
-      for (int t = 0; ok && t < T; ++t) {
-        ok = wait_w(t) && (t + 2 >= T || wait_sg(t + 2));
-        if (!ok) break;
-        tc_fence_after();
-        issue_w(t);
-        if (t + 2 < T) issue_sg(t + 2);
+      // Issue blocks until the tensor pipe has taken all but the last few
+      // MMAs of a burst, so each wait between bursts leaves the pipe that
+      // little work to run on.  At d = 128 the waits are spread out: K of
+      // tile t + 2 is awaited behind the W MMAs of tile t, V of tile t + 1
+      // and the elementwise warps' P of tile t + 1 behind the S/G MMAs of
+      // tile t + 2 (measured 4.05 -> 3.72 ms at B=2, H=16, N=16384).  At
+      // d = 64, whose bursts are half as long, all waits of a tile before its
+      // MMAs measured faster.
+      if (D == 128) {
+        if (ok && T > 0) ok = wait_v(0);
+        for (int t = 0; ok && t < T; ++t) {
+          if (!wait_p(t)) { ok = false; break; }
+          tc_fence_after();
+          issue_w(t);
+          if (t + 2 < T) {
+            if (!wait_sg(t + 2)) { ok = false; break; }
+            tc_fence_after();
+            issue_sg(t + 2);
+          }
+          if (t + 1 < T && !wait_v(t + 1)) { ok = false; break; }
+        }
+      } else {
+        for (int t = 0; ok && t < T; ++t) {
+          ok = wait_p(t) && wait_v(t) && (t + 2 >= T || wait_sg(t + 2));
+          if (!ok) break;
+          tc_fence_after();
+          issue_w(t);
+          if (t + 2 < T) issue_sg(t + 2);
+        }
       }
       if (ok) mma_commit_w(w_done);
       // every MMA this thread issued has completed before TMEM is released
