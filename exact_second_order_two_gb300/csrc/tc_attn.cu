@@ -703,13 +703,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto reduce_dq = [&](int t, const uint32_t (&dq)[NC]) {
       const int qa = qstart + rotated(t, rot, T) * C::BN + NC * slice;
       if (D == 128) {
-        red_columns<NC>(prm.acc + ((size_t)bh * N + qa) * D + row, D, dq, N - qa);
+        red_columns<D, NC>(prm.acc + ((size_t)bh * N + qa) * D + row, dq, N - qa);
       } else {
         // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
         // lanes 32w' + x; the upper 16 lanes of each warp hold nothing
         if (lane < 16) {
-          red_columns<NC>(prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane, D, dq,
-                          N - qa);
+          red_columns<D, NC>(prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane, dq, N - qa);
         }
       }
     };

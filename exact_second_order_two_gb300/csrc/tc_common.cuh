@@ -102,20 +102,19 @@ inline int cta_group_heads(int BH, int nblk, int sms) {
   return G < BH ? G : BH;
 }
 
-// Adds this thread's NC fp32 partials (consecutive columns, `stride`
-// elements apart in the accumulator) with one global reduction each; only the
-// first `valid` are inside the sequence.  The scale factor of dQ / gradQ is
-// applied once, when the accumulator is converted to bf16.
-template <int NC>
-__device__ __forceinline__ void red_columns(float* base, size_t stride, const uint32_t (&v)[NC],
-                                            int valid) {
+// Adds this thread's NC fp32 partials (consecutive columns, STRIDE elements
+// apart in the accumulator) with one global reduction each; only the first
+// `valid` are inside the sequence.  The scale factor of dQ / gradQ is applied
+// once, when the accumulator is converted to bf16.
+template <int STRIDE, int NC>
+__device__ __forceinline__ void red_columns(float* base, const uint32_t (&v)[NC], int valid) {
   if (valid >= NC) {
 #pragma unroll
-    for (int c = 0; c < NC; ++c) atomicAdd(base + (size_t)c * stride, __uint_as_float(v[c]));
+    for (int c = 0; c < NC; ++c) atomicAdd(base + (size_t)c * STRIDE, __uint_as_float(v[c]));
   } else {
 #pragma unroll
     for (int c = 0; c < NC; ++c)
-      if (c < valid) atomicAdd(base + (size_t)c * stride, __uint_as_float(v[c]));
+      if (c < valid) atomicAdd(base + (size_t)c * STRIDE, __uint_as_float(v[c]));
   }
 }
 
