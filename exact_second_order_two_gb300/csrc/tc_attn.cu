@@ -421,7 +421,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 template <int D>
 struct Bwd {
   static constexpr int BM = 128, BN = 64;
-  static constexpr int STAGES = 2, DSTAGES = 2;  // Q (+ row scalars) ring, dO ring
+  // Q (+ row scalars) ring and dO ring: three stages each, because the next
+  // tile's S^T and dP^T are issued while this tile's elementwise phase runs,
+  // before this tile's dK / dV MMAs have released its Q and dO
+  static constexpr int STAGES = 3, DSTAGES = 3;
   static constexpr uint32_t KB = BM * D * 2;     // stationary K, V tile
   static constexpr uint32_t QB = BN * D * 2;     // streamed Q, dO tile
   static constexpr uint32_t XB = BM * BN * 2;    // dS^T tile (dQ^T B operand)
@@ -433,13 +436,16 @@ struct Bwd {
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "backward shared memory budget");
-  // TMEM columns.  After the elementwise warps have read a tile's scores they
-  // write, inside the 16 S^T columns each of them read, bf16 P^T (first 8)
-  // and dS^T (last 8): the A operands of the dV / dK MMAs.  The dP^T columns
-  // are then free for the next tile's dP^T, issued while the elementwise
-  // phase runs.
-  static constexpr uint32_t T_S = 0, T_DP = 64, T_DK = 128, T_DV = 128 + D, T_DQ = 128 + 2 * D;
-  static constexpr bool EARLY_DP = true;
+  // TMEM columns.  S^T has two buffers, so the next tile's S^T (and dP^T,
+  // once its predecessor has been read out) is computed while the
+  // elementwise warps work on this tile: they start the next tile as soon
+  // as they are done with this one, and the dK / dV / dQ^T MMAs of a tile
+  // run during the next tile's elementwise phase.  After reading a tile's
+  // scores the elementwise warps write, inside the 16 S^T columns each of
+  // them read, bf16 P^T (first 8) and dS^T (last 8): the A operands of the
+  // dV / dK MMAs.
+  __host__ __device__ static constexpr uint32_t T_S(int b) { return 64u * b; }
+  static constexpr uint32_t T_DP = 128, T_DK = 192, T_DV = 192 + D, T_DQ = 192 + 2 * D;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(T_DQ + 64 <= TMEM_COLS, "backward TMEM budget");
 };
@@ -482,13 +488,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* q_empty = q_full + C::STAGES;       // [STAGES]: dK MMAs done with Q
   uint64_t* do_full = q_empty + C::STAGES;      // [DSTAGES]
   uint64_t* do_empty = do_full + C::DSTAGES;    // [DSTAGES]: dV MMAs done with dO
-  uint64_t* sc_full = do_empty + C::DSTAGES;
-  uint64_t* sc_read = sc_full + 1;              // elementwise warps hold the scores
-  uint64_t* ds_full = sc_read + 1;
+  uint64_t* s_full = do_empty + C::DSTAGES;     // [2]: S^T of a buffer in TMEM
+  uint64_t* dp_full = s_full + 2;               // dP^T in TMEM
+  uint64_t* dp_read = dp_full + 1;              // elementwise warps hold S^T and dP^T
+  uint64_t* ds_full = dp_read + 1;
   uint64_t* dq_full = ds_full + 1;
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* acc_done = dq_empty + 1;
   uint64_t* drain = acc_done + 1;
+  static_assert((11 + 2 * C::STAGES + 2 * C::DSTAGES) * 8 <= 256,
+                "barriers end below the TMEM slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
   Abort* abort_st = reinterpret_cast<Abort*>(smem + C::OFF_MISC + 264);
   float* scal = reinterpret_cast<float*>(smem + C::OFF_SC);
@@ -512,8 +521,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(do_full + s, 1);
       mbar_init(do_empty + s, 1);
     }
-    mbar_init(sc_full, 1);
-    mbar_init(sc_read, kBwdConsumers);
+    mbar_init(s_full, 1);
+    mbar_init(s_full + 1, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(dp_read, kBwdConsumers);
     mbar_init(ds_full, kBwdConsumers);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, kBwdConsumers);
@@ -606,9 +617,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t k_lo = lo_kmajor(sb + C::OFF_K), v_lo = lo_kmajor(sb + C::OFF_V);
       const uint32_t k_mn = lo_mnmajor(sb + C::OFF_K, C::BM * 128);
       const uint32_t ds_mn = lo_mnmajor(sb + C::OFF_DS, 1024);
-      const uint32_t t_s = tmem + C::T_S, t_dp = tmem + C::T_DP, t_dk = tmem + C::T_DK,
-                     t_dv = tmem + C::T_DV, t_dq = tmem + C::T_DQ;
-      // dP^T of tile t (needs dO(t) and the previous tile's dP^T read out)
+      const uint32_t t_dp = tmem + C::T_DP, t_dk = tmem + C::T_DK, t_dv = tmem + C::T_DV,
+                     t_dq = tmem + C::T_DQ;
+      // dP^T of tile t (needs dO(t) and the previous tile's dP^T read out),
+      // then its commit
       auto issue_dp = [&](int t) -> bool {
         const int ds = t % C::DSTAGES;
         const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
@@ -619,36 +631,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int k = 0; k < D / 16; ++k)
           mma_ss_w(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
                  k > 0 ? 1u : 0u);
+        mma_commit_w(dp_full);
         return true;
       };
-      // S^T of tile t (needs Q(t); overwrites the A operands of tile t - 1),
-      // then the commit that covers both score blocks
+      // S^T of tile t into buffer t & 1 (needs Q(t); overwrites the A
+      // operands of tile t - 2, whose dK / dV MMAs were issued before), then
+      // its commit
       auto issue_s = [&](int t) -> bool {
         const int s = t % C::STAGES;
         const uint32_t q_lo = opaque(lo_kmajor(sb + C::OFF_Q + s * C::QB));
         const uint32_t k_l = opaque(k_lo);
         if (!warp_wait(q_full + s, (t / C::STAGES) & 1, abort_st, prm.status)) return false;
         tc_fence_after();
+        const uint32_t t_s = tmem + C::T_S(t & 1);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_ss_w(t_s, k_l + kslice_off(C::BM, k), q_lo + kslice_off(C::BN, k), id_sc,
                  k > 0 ? 1u : 0u);
-        mma_commit_w(sc_full);
+        mma_commit_w(s_full + (t & 1));
         return true;
       };
       bool ok = warp_wait(kv_full, 0, abort_st, prm.status) && issue_dp(0) && issue_s(0);
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES, ds = t % C::DSTAGES;
-        if (C::EARLY_DP && t + 1 < T) {
-          if (!warp_wait(sc_read, t & 1, abort_st, prm.status)) { ok = false; break; }
+        // ---- next tile's dP^T and S^T while the elementwise warps work ----
+        if (t + 1 < T) {
+          if (!warp_wait(dp_read, t & 1, abort_st, prm.status)) { ok = false; break; }
           tc_fence_after();
-          if (!issue_dp(t + 1)) { ok = false; break; }
+          if (!issue_dp(t + 1) || !issue_s(t + 1)) { ok = false; break; }
         }
         if (!warp_wait(ds_full, t & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
         {
           const uint32_t q_mn = opaque(lo_mnmajor(sb + C::OFF_Q + s * C::QB, C::BN * 128));
           const uint32_t do_mn = opaque(lo_mnmajor(sb + C::OFF_DO + ds * C::QB, C::BN * 128));
+          const uint32_t t_s = tmem + C::T_S(t & 1);
           const uint32_t first = t > 0 ? 1u : 0u;
           // dK += dS^T Q first: it releases the Q stage
 #pragma unroll
@@ -660,11 +677,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_ts_w(t_dv, t_s + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
           mma_commit_w(do_empty + ds);
         }
-        // the next tile's scores overwrite the A operands read above (MMAs
-        // from one thread run in issue order); its elementwise phase then
-        // overlaps this tile's dQ^T
-        if (!C::EARLY_DP && t + 1 < T && !issue_dp(t + 1)) { ok = false; break; }
-        if (t + 1 < T && !issue_s(t + 1)) { ok = false; break; }
+        // dQ^T of tile t, once the previous one has been read out of TMEM;
+        // it runs during the next tile's elementwise phase, which drains it
         if (t >= 1) {
           if (!warp_wait(dq_empty, (t - 1) & 1, abort_st, prm.status)) { ok = false; break; }
           tc_fence_after();
@@ -716,16 +730,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
       const int q0 = qstart + rotated(t, rot, T) * C::BN;
-      if (!warp_wait(sc_full, t & 1, abort_st, prm.status)) { ok = false; break; }
+      if (!warp_wait(s_full + (t & 1), (t >> 1) & 1, abort_st, prm.status) ||
+          !warp_wait(dp_full, t & 1, abort_st, prm.status)) {
+        ok = false;
+        break;
+      }
       if (!warp_wait(q_full + s, (t / C::STAGES) & 1, abort_st, prm.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[NC], dpr[NC];
       const uint32_t tl = tmem + lane_off + NC * slice;
-      tmem_ld16x2(tl + C::T_S, tl + C::T_DP, sr, dpr);
-      if (C::EARLY_DP) {  // the loads above have completed: dP^T is free
-        tc_fence_before();
-        mbar_arrive(sc_read);
-      }
+      const uint32_t ts = tl + C::T_S(t & 1);
+      tmem_ld16x2(ts, tl + C::T_DP, sr, dpr);
+      // the loads above have completed: the dP^T columns are free
+      tc_fence_before();
+      mbar_arrive(dp_read);
       const float4* sc4 = reinterpret_cast<const float4*>(scal + s * 2 * C::BN + NC * slice);
       const int qa = q0 + NC * slice;
       const bool need_mask = (qa + NC > N) || (j0 + C::BM > N) || (prm.causal && qa < j0 + C::BM);
@@ -759,7 +777,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // A operands of the dV / dK MMAs: bf16 pairs (low half = even query),
       // P^T in the first 8 and dS^T in the last 8 of the 16 S^T columns this
       // thread read
-      tmem_st8x2(tl + C::T_S, pw, tl + C::T_S + 8, dsw);
+      tmem_st8x2(ts, pw, ts + 8, dsw);
       // the previous tile's dQ^T MMAs read the dS^T tile below: drain their
       // result first
       uint32_t dq[NC];
