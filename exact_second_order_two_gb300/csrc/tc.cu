@@ -52,7 +52,13 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+// Waits for a tile's operands (P from the elementwise warps, V and the K two
+// tiles ahead from TMA) and signals them to the MMA warp as one barrier: an
+// mbarrier test by the MMA warp costs hundreds of cycles while the tensor
+// pipe streams its operands, and the pipe holds only a few MMAs of work to
+// cover it, so one wait per tile leaves it idle far less than three.
+constexpr int kHelperWarp = 10;
+constexpr int kThreads = 352;
 constexpr int kConsumers = kConsumerWarps * 32;
 __device__ __forceinline__ void consumer_sync() { named_sync<kConsumers>(1); }
 
@@ -155,6 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* w_done = p_full + 2;
   uint64_t* q_tmem = w_done + 2;                  // Q, gQ copied into TMEM
   uint64_t* drain = w_done + 1;
+  uint64_t* ready = q_tmem + 1;                   // [2]: P(t), V(t), K(t+2) all in place
+  static_assert((1 + 2 * C::STAGES + 2 * C::VSTAGES + 9) * 8 <= 256,
+                "barriers end below the TMEM slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
   Abort* abort_st = reinterpret_cast<Abort*>(smem + C::OFF_MISC + 264);
   float* part = reinterpret_cast<float*>(smem + C::OFF_PART);
@@ -188,6 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(w_done, 1);
     mbar_init(drain, 1);
     mbar_init(q_tmem, kConsumers);
+    mbar_init(ready, 1);
+    mbar_init(ready + 1, 1);
     abort_st->flag = 0;
     abort_st->limit_ns = prm.wait_ns;
     fence_mbar_init();
@@ -263,12 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_sg = [&](int t) -> bool {
         return warp_wait(kg_full + t % C::STAGES, (t / C::STAGES) & 1, abort_st, prm.status);
       };
-      auto wait_p = [&](int t) -> bool {
-        return warp_wait(p_full + (t & 1), (t >> 1) & 1, abort_st, prm.status);
-      };
-      auto wait_v = [&](int t) -> bool {
-        return warp_wait(v_full + t % C::VSTAGES, (t / C::VSTAGES) & 1, abort_st, prm.status);
-      };
       auto issue_sg = [&](int t) {
         const int s = t % C::STAGES, b = t & 1;
         // [K;gK] per half, 2*BN rows
@@ -318,40 +323,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_sg(t);
         }
       }
-      // Issue blocks until the tensor pipe has taken all but the last few
-      // MMAs of a burst, so each wait between bursts leaves the pipe that
-      // little work to run on.  At d = 128 the waits are spread out: K of
-      // tile t + 2 is awaited behind the W MMAs of tile t, V of tile t + 1
-      // and the elementwise warps' P of tile t + 1 behind the S/G MMAs of
-      // tile t + 2 (measured 4.05 -> 3.72 ms at B=2, H=16, N=16384).  At
-      // d = 64, whose bursts are half as long, all waits of a tile before its
-      // MMAs measured faster.
-      if (D == 128) {
-        if (ok && T > 0) ok = wait_v(0);
-        for (int t = 0; ok && t < T; ++t) {
-          if (!wait_p(t)) { ok = false; break; }
-          tc_fence_after();
-          issue_w(t);
-          if (t + 2 < T) {
-            if (!wait_sg(t + 2)) { ok = false; break; }
-            tc_fence_after();
-            issue_sg(t + 2);
-          }
-          if (t + 1 < T && !wait_v(t + 1)) { ok = false; break; }
-        }
-      } else {
-        for (int t = 0; ok && t < T; ++t) {
-          ok = wait_p(t) && wait_v(t) && (t + 2 >= T || wait_sg(t + 2));
-          if (!ok) break;
-          tc_fence_after();
-          issue_w(t);
-          if (t + 2 < T) issue_sg(t + 2);
-        }
+      // One wait per tile, on the helper warp's combined barrier.  Tile t's
+      // phase of ready[t & 1] cannot be signalled before the MMA warp has
+      // passed its wait for tile t - 2: the helper first needs P(t), which
+      // needs S(t), issued only after that wait.
+      for (int t = 0; ok && t < T; ++t) {
+        if (!warp_wait(ready + (t & 1), (t >> 1) & 1, abort_st, prm.status)) { ok = false; break; }
+        tc_fence_after();
+        issue_w(t);
+        if (t + 2 < T) issue_sg(t + 2);
       }
       if (ok) mma_commit_w(w_done);
       // every MMA this thread issued has completed before TMEM is released
       mma_commit_w(drain);
       mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
+    }
+  } else if (warp == kHelperWarp) {
+    if (lane == 0) {
+      for (int t = 0; t < T; ++t) {
+        if (!wait_bar(p_full + (t & 1), (t >> 1) & 1, abort_st, prm.status) ||
+            !wait_bar(v_full + t % C::VSTAGES, (t / C::VSTAGES) & 1, abort_st, prm.status) ||
+            (t + 2 < T && !wait_bar(kg_full + (t + 2) % C::STAGES, ((t + 2) / C::STAGES) & 1,
+                                    abort_st, prm.status)))
+          break;
+        mbar_arrive(ready + (t & 1));
+      }
     }
   } else {
     // ---------------- elementwise warps: thread = query row --------------
