@@ -528,9 +528,6 @@ struct Col {
   // inside the 16 columns each thread read: gS^T into the first 8 and dS^T
   // into the last 8 of S^T, gdP^T into the first 8 of G^T.
   static constexpr uint32_t T_S = 0, T_G = 64, T_DP = 128, T_H = 192, T_GK = 256, T_GV = 256 + D;
-  // The next tile's dP^T, H^T are issued as soon as the scores have been
-  // read, so that they run during the elementwise phase.
-  static constexpr bool EARLY_DH = true;
   // gradQ^T partial (64 columns): its own region when TMEM has room (d = 64),
   // else the S^T columns, which the next tile rewrites last (d = 128)
   static constexpr bool GQ_IN_S = (256 + 2 * D + 64 > 512);
@@ -540,6 +537,13 @@ struct Col {
   // elementwise warps drain the partial one tile late.
   static constexpr bool LATE_GQ = !GQ_IN_S;
   static constexpr uint32_t TMEM_COLS = 512;
+  // At d = 64 a helper warp folds pairs of the MMA warp's waits into one
+  // barrier each (as in pass 1): (scores read, next dO landed) before the
+  // next tile's dP^T / H^T, and (next [Q|gQ] landed, previous gradQ^T
+  // partial drained) before its S^T / G^T.  At d = 128 the score read-out
+  // and the gradQ^T drain are the last events before the MMAs they gate, and
+  // a hop through another warp adds its wake-up to every tile.
+  static constexpr bool HELPER = !GQ_IN_S;
 };
 
 struct ColParams {
@@ -566,18 +570,21 @@ struct ColParams {
 // warp of its own so that its loads run as far ahead as its ring allows:
 // the next tile's dP^T / H^T MMAs wait for it while the elementwise phase
 // runs, and the [Q|gQ] producer spends most of each tile waiting for the
-// gradK MMAs to free its stage.
+// gradK MMAs to free its stage.  Warp 19, at d = 64 only, is the helper
+// (Col::HELPER).
 constexpr int kColConsumerWarps = 16;
 constexpr int kColConsumers = kColConsumerWarps * 32;
 constexpr int kColProducerWarp = kColConsumerWarps;
 constexpr int kColMmaWarp = kColConsumerWarps + 1;
 constexpr int kColDoWarp = kColConsumerWarps + 2;
-constexpr int kColThreads = (kColConsumerWarps + 3) * 32;
+constexpr int kColHelperWarp = kColConsumerWarps + 3;
+template <int D>
+constexpr int col_threads() { return (kColConsumerWarps + (Col<D>::HELPER ? 4 : 3)) * 32; }
 constexpr int kColCols = 64 / (kColConsumerWarps / 4);  // columns per elementwise thread
 static_assert(kColCols == 16, "one 16-query MMA step per column slice");
 
 template <int D, bool ALL>
-__global__ void __launch_bounds__(kColThreads, 1)
+__global__ void __launch_bounds__(col_threads<D>(), 1)
     bob_col_pass(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mGK,
                  const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mGV,
                  const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mGQ,
@@ -606,7 +613,9 @@ __global__ void __launch_bounds__(kColThreads, 1)
   uint64_t* gq_empty = gq_full + 1;
   uint64_t* acc_done = gq_empty + 1;
   uint64_t* drain = acc_done + 1;
-  static_assert((8 + 2 * C::STAGES + 2 * C::DSTAGES) * 8 <= 256,
+  uint64_t* ready_dh = drain + 1;               // [2] (HELPER): next tile's dP^T / H^T may go
+  uint64_t* ready_sg = ready_dh + 2;            // [2] (HELPER): next tile's S^T / G^T may go
+  static_assert((12 + 2 * C::STAGES + 2 * C::DSTAGES) * 8 <= 256,
                 "barriers end below the TMEM slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
   Abort* abort_st = reinterpret_cast<Abort*>(smem + C::OFF_MISC + 264);
@@ -638,6 +647,12 @@ __global__ void __launch_bounds__(kColThreads, 1)
     mbar_init(gq_empty, kColConsumers);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
+    if (C::HELPER) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(ready_dh + b, 1);
+        mbar_init(ready_sg + b, 1);
+      }
+    }
     abort_st->flag = 0;
     abort_st->limit_ns = prm.wait_ns;
     fence_mbar_init();
@@ -740,6 +755,24 @@ __global__ void __launch_bounds__(kColThreads, 1)
         mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
                           100000000ull);
     }
+  } else if (warp == kColHelperWarp) {
+    if (C::HELPER && lane == 0) {
+      for (int t = 0; t + 1 < T; ++t) {
+        const int u = t + 1;
+        // dP^T / H^T of tile u: tile t's scores read out, dO(u) landed
+        if (!wait_bar(sc_read, t & 1, abort_st, prm.status) ||
+            !wait_bar(do_full + u % C::DSTAGES, (u / C::DSTAGES) & 1, abort_st, prm.status))
+          break;
+        mbar_arrive(ready_dh + (t & 1));
+        // S^T / G^T of tile u: [Q|gQ](u) landed (with its row scalars), and
+        // the gradQ^T partial that the gradQ^T MMAs after them replace (tile
+        // t - 1's) read out
+        if (!wait_bar(qg_full + u % C::STAGES, (u / C::STAGES) & 1, abort_st, prm.status) ||
+            (t >= 1 && !wait_bar(gq_empty, (t - 1) & 1, abort_st, prm.status)))
+          break;
+        mbar_arrive(ready_sg + (t & 1));
+      }
+    }
   } else if (warp == kColMmaWarp) {
     {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
       constexpr uint32_t id_sc = idesc_bf16(128, 64, false, false);  // scores: M=128 N=64
@@ -758,11 +791,12 @@ __global__ void __launch_bounds__(kColThreads, 1)
                      t_gq = tmem + C::T_GQ;
       // dP^T and H^T of tile t (need dO(t) and the previous tile's scores
       // read out of TMEM)
-      auto issue_dh = [&](int t) -> bool {
+      auto issue_dh = [&](int t, bool wait) -> bool {
         const int ds = t % C::DSTAGES;
         const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
         const uint32_t v_l = opaque(v_lo), gv_l = opaque(gv_lo);
-        if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_st, prm.status)) return false;
+        if (wait && !warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_st, prm.status))
+          return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
@@ -778,11 +812,12 @@ __global__ void __launch_bounds__(kColThreads, 1)
       // S^T and G^T of tile t (need Q, gQ; overwrite the A operands of tile
       // t - 1 and, at d = 128, its gradQ^T partial), then the commit that
       // covers all four score blocks
-      auto issue_sg = [&](int t) -> bool {
+      auto issue_sg = [&](int t, bool wait) -> bool {
         const int s = t % C::STAGES;
         const uint32_t qgq_lo = opaque(lo_kmajor(sb + C::OFF_QG + s * 2 * C::QB));  // [Q;gQ] per half
         const uint32_t k_l = opaque(k_lo), gk_l = opaque(gk_lo);
-        if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_st, prm.status)) return false;
+        if (wait && !warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_st, prm.status))
+          return false;
         if (C::GQ_IN_S && t >= 1 && !warp_wait(gq_empty, (t - 1) & 1, abort_st, prm.status))
           return false;
         tc_fence_after();
@@ -803,14 +838,22 @@ __global__ void __launch_bounds__(kColThreads, 1)
         mma_commit_w(sc_full);
         return true;
       };
-      bool ok = warp_wait(kv_full, 0, abort_st, prm.status) && issue_dh(0) && issue_sg(0);
+      // With the helper, loop iteration t waits on phase t >> 1 of
+      // ready_dh[t & 1] and ready_sg[t & 1], the helper's arrivals for tile
+      // t + 1.  Its arrival for tile t + 3 on the same barriers cannot come
+      // before that wait has passed: the helper first needs the scores of
+      // tile t + 2 read out, and S^T(t + 2) is issued by iteration t + 1.
+      bool ok = warp_wait(kv_full, 0, abort_st, prm.status) && issue_dh(0, true) &&
+                issue_sg(0, true);
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES, ds = t % C::DSTAGES;
         // ---- next tile's dP^T, H^T while the elementwise warps work ----
-        if (C::EARLY_DH && t + 1 < T) {
-          if (!warp_wait(sc_read, t & 1, abort_st, prm.status)) { ok = false; break; }
+        if (t + 1 < T) {
+          const bool w = C::HELPER ? warp_wait(ready_dh + (t & 1), (t >> 1) & 1, abort_st, prm.status)
+                                   : warp_wait(sc_read, t & 1, abort_st, prm.status);
+          if (!w) { ok = false; break; }
           tc_fence_after();
-          if (!issue_dh(t + 1)) { ok = false; break; }
+          if (!issue_dh(t + 1, !C::HELPER)) { ok = false; break; }
         }
         // ---- outputs: A operands (bf16 gS^T, dS^T, gdP^T) from TMEM ----
         if (!warp_wait(ds_full, t & 1, abort_st, prm.status)) { ok = false; break; }
@@ -833,7 +876,9 @@ __global__ void __launch_bounds__(kColThreads, 1)
         // d = 128 it overwrites S^T, whose A operands the gradK MMAs above
         // read first (MMAs from one thread run in issue order)
         auto issue_gq = [&]() -> bool {
-          if (!C::GQ_IN_S && t >= 1) {
+          // with the helper this wait is part of ready_sg, awaited just
+          // before, except on the last tile, which has no next tile
+          if (!C::GQ_IN_S && t >= 1 && (!C::HELPER || t + 1 >= T)) {
             if (!warp_wait(gq_empty, (t - 1) & 1, abort_st, prm.status)) return false;
             tc_fence_after();
           }
@@ -854,9 +899,13 @@ __global__ void __launch_bounds__(kColThreads, 1)
         for (int k = 0; k < C::BN / 16; ++k)
           mma_ts_w(t_gv, t_g + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
         mma_commit_w(do_empty + ds);
-        // without EARLY_DH, ds_full (all scores read) has already freed dP^T, H^T
-        if (!C::EARLY_DH && t + 1 < T && !issue_dh(t + 1)) { ok = false; break; }
-        if (t + 1 < T && !issue_sg(t + 1)) { ok = false; break; }
+        if (t + 1 < T) {
+          if (C::HELPER && !warp_wait(ready_sg + (t & 1), (t >> 1) & 1, abort_st, prm.status)) {
+            ok = false;
+            break;
+          }
+          if (!issue_sg(t + 1, !C::HELPER)) { ok = false; break; }
+        }
         if (C::LATE_GQ && !issue_gq()) { ok = false; break; }
       }
       if (ok) mma_commit_w(acc_done);
@@ -904,10 +953,9 @@ __global__ void __launch_bounds__(kColThreads, 1)
       uint32_t sr[NC], dpr[NC], gr[NC], hr[NC];
       const uint32_t tl = tmem + lane_off + NC * slice;
       tmem_ld16x4(tl + C::T_S, tl + C::T_DP, tl + C::T_G, tl + C::T_H, sr, dpr, gr, hr);
-      if (C::EARLY_DH) {  // the loads above have completed: dP^T, H^T are free
-        tc_fence_before();
-        mbar_arrive(sc_read);
-      }
+      // the loads above have completed: dP^T, H^T are free
+      tc_fence_before();
+      mbar_arrive(sc_read);
       const float4* sc4 =
           reinterpret_cast<const float4*>(scal + (t % C::SCSTAGES) * 4 * C::BN + NC * slice);
       const int qa = q0 + NC * slice;
@@ -1128,7 +1176,7 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
   cp.has_gk = has_gk;
   cp.has_gv = has_gv;
   dim3 g2((unsigned)(((p.N + Cc::BM - 1) / Cc::BM) * p.BH()));
-  col_kernel<<<g2, kColThreads, Cc::SMEM, log.stream>>>(mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc, cp);
+  col_kernel<<<g2, col_threads<D>(), Cc::SMEM, log.stream>>>(mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc, cp);
   e = cudaGetLastError();
   log.mark();
   if (e != cudaSuccess) return e;
