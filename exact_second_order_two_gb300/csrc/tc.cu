@@ -503,8 +503,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 struct Col {
   static constexpr int BM = 128, BN = 64;
-  static constexpr int STAGES = D == 128 ? 1 : 2;    // [Q|gQ] (+ row scalars) ring
-  static constexpr int DSTAGES = 2;                  // dO ring
+  // At d = 64 two score buffers (SG2 below) put the next tile's S^T / G^T
+  // ahead of this tile's gradK / gradV, so both rings hold three tiles.
+  static constexpr int STAGES = D == 128 ? 1 : 3;    // [Q|gQ] (+ row scalars) ring
+  static constexpr int DSTAGES = D == 128 ? 2 : 3;   // dO ring
   static constexpr uint32_t KB = BM * D * 2;     // stationary K, gK, V, gV tile
   static constexpr uint32_t QB = BN * D * 2;     // streamed Q, gQ, dO tile
   static constexpr uint32_t XB = BM * BN * 2;    // dS^T / gS^T tile (gradQ^T B operands)
@@ -526,24 +528,33 @@ struct Col {
   // tile's dP^T and H^T are computed into their columns while the
   // elementwise phase runs.  The bf16 A operands of the gradK / gradV MMAs go
   // inside the 16 columns each thread read: gS^T into the first 8 and dS^T
-  // into the last 8 of S^T, gdP^T into the first 8 of G^T.
-  static constexpr uint32_t T_S = 0, T_G = 64, T_DP = 128, T_H = 192, T_GK = 256, T_GV = 256 + D;
-  // gradQ^T partial (64 columns): its own region when TMEM has room (d = 64),
-  // else the S^T columns, which the next tile rewrites last (d = 128)
-  static constexpr bool GQ_IN_S = (256 + 2 * D + 64 > 512);
-  static constexpr uint32_t T_GQ = GQ_IN_S ? T_S : 256 + 2 * D;
-  // With its own region the gradQ^T MMAs of a tile follow the next tile's
-  // scores, so they run during that tile's elementwise phase, and the
-  // elementwise warps drain the partial one tile late.
-  static constexpr bool LATE_GQ = !GQ_IN_S;
+  // into the last 8 of S^T, gdP^T into the first 8 of G^T.  The gradQ^T
+  // partial of a tile (64 columns) goes into its S^T columns once the gradK
+  // MMAs have read them.
+  // d = 128: one S^T / G^T buffer.  The MMA order per tile is gradK, gradQ^T,
+  // gradV, then the next tile's S^T / G^T, which wait for the elementwise
+  // warps to drain the partial at the end of their tile.
+  // d = 64 (SG2): TMEM also holds a second S^T / G^T buffer (tile t in
+  // buffer t % 2).  The next tile's S^T / G^T go first, into the other
+  // buffer, as soon as the elementwise warps have drained the partial of
+  // the tile before (which they do as they hand over this tile's A
+  // operands), so they run while those warps reduce that partial; then
+  // gradK, gradV and gradQ^T of this tile, during the next tile's
+  // elementwise phase.
+  static constexpr bool SG2 = (D == 64);
+  __host__ __device__ static constexpr uint32_t T_S(int b) { return SG2 ? 128u * b : 0u; }
+  __host__ __device__ static constexpr uint32_t T_G(int b) { return T_S(b) + 64u; }
+  static constexpr uint32_t T_DP = SG2 ? 256 : 128, T_H = T_DP + 64, T_GK = T_H + 64,
+                            T_GV = T_GK + D;
+  static_assert(T_GV + D == 512, "pass 2 TMEM layout fills 512 columns");
   static constexpr uint32_t TMEM_COLS = 512;
   // At d = 64 a helper warp folds pairs of the MMA warp's waits into one
   // barrier each (as in pass 1): (scores read, next dO landed) before the
-  // next tile's dP^T / H^T, and (next [Q|gQ] landed, previous gradQ^T
-  // partial drained) before its S^T / G^T.  At d = 128 the score read-out
-  // and the gradQ^T drain are the last events before the MMAs they gate, and
-  // a hop through another warp adds its wake-up to every tile.
-  static constexpr bool HELPER = !GQ_IN_S;
+  // next tile's dP^T / H^T, and (next [Q|gQ] landed, gradQ^T partial of the
+  // tile before drained) before its S^T / G^T.  At d = 128 the score
+  // read-out and the gradQ^T drain are the last events before the MMAs they
+  // gate, and a hop through another warp adds its wake-up to every tile.
+  static constexpr bool HELPER = SG2;
 };
 
 struct ColParams {
@@ -786,9 +797,8 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
       const uint32_t k_mn = lo_mnmajor(sb + C::OFF_K, C::BM * 128),
                      gk_mn = lo_mnmajor(sb + C::OFF_GK, C::BM * 128);
       const uint32_t ds_mn = lo_mnmajor(sb + C::OFF_DS, 1024), gs_mn = lo_mnmajor(sb + C::OFF_GS, 1024);
-      const uint32_t t_s = tmem + C::T_S, t_g = tmem + C::T_G, t_dp = tmem + C::T_DP,
-                     t_h = tmem + C::T_H, t_gk = tmem + C::T_GK, t_gv = tmem + C::T_GV,
-                     t_gq = tmem + C::T_GQ;
+      const uint32_t t_dp = tmem + C::T_DP, t_h = tmem + C::T_H, t_gk = tmem + C::T_GK,
+                     t_gv = tmem + C::T_GV;
       // dP^T and H^T of tile t (need dO(t) and the previous tile's scores
       // read out of TMEM)
       auto issue_dh = [&](int t, bool wait) -> bool {
@@ -809,16 +819,20 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
         }
         return true;
       };
-      // S^T and G^T of tile t (need Q, gQ; overwrite the A operands of tile
-      // t - 1 and, at d = 128, its gradQ^T partial), then the commit that
-      // covers all four score blocks
+      // S^T and G^T of tile t into buffer t % 2 (need Q, gQ; overwrite the
+      // A operands and the gradQ^T partial of the tile that last used the
+      // buffer: t - 1 at d = 128, t - 2 with SG2), then the commit that
+      // covers all four score blocks.  With the helper, wait = false: its
+      // barrier covered both waits.
       auto issue_sg = [&](int t, bool wait) -> bool {
         const int s = t % C::STAGES;
         const uint32_t qgq_lo = opaque(lo_kmajor(sb + C::OFF_QG + s * 2 * C::QB));  // [Q;gQ] per half
         const uint32_t k_l = opaque(k_lo), gk_l = opaque(gk_lo);
+        const uint32_t t_s = tmem + C::T_S(t & 1), t_g = tmem + C::T_G(t & 1);
+        const int prev = C::SG2 ? t - 2 : t - 1;  // the buffer's previous tile
         if (wait && !warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_st, prm.status))
           return false;
-        if (C::GQ_IN_S && t >= 1 && !warp_wait(gq_empty, (t - 1) & 1, abort_st, prm.status))
+        if (wait && prev >= 0 && !warp_wait(gq_empty, prev & 1, abort_st, prm.status))
           return false;
         tc_fence_after();
         // [S^T | K gQ^T] = K [Q; gQ]^T (S^T = K Q^T alone without gQ), then
@@ -855,9 +869,17 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
           tc_fence_after();
           if (!issue_dh(t + 1, !C::HELPER)) { ok = false; break; }
         }
+        // ---- SG2: next tile's S^T, G^T into the other buffer ----
+        auto next_sg = [&]() -> bool {
+          if (C::HELPER && !warp_wait(ready_sg + (t & 1), (t >> 1) & 1, abort_st, prm.status))
+            return false;
+          return issue_sg(t + 1, !C::HELPER);
+        };
+        if (C::SG2 && t + 1 < T && !next_sg()) { ok = false; break; }
         // ---- outputs: A operands (bf16 gS^T, dS^T, gdP^T) from TMEM ----
         if (!warp_wait(ds_full, t & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t t_s = tmem + C::T_S(t & 1), t_g = tmem + C::T_G(t & 1);
         const uint32_t qgq_s = sb + C::OFF_QG + s * 2 * C::QB;
         // B operands MN-major: 64-feature groups 2*BN*128 bytes apart in the
         // interleaved [Q;gQ] stage, BN*128 apart in the dO tile
@@ -872,41 +894,33 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
           if (has_gq) mma_ts_w(t_gk, t_s + 16 * k + 8, gq_mn + kstep_off(k), id_out, 1u);
         }
         mma_commit_w(qg_empty + s);
-        // gradQ^T of tile t, once the previous partial has been drained; at
-        // d = 128 it overwrites S^T, whose A operands the gradK MMAs above
-        // read first (MMAs from one thread run in issue order)
-        auto issue_gq = [&]() -> bool {
-          // with the helper this wait is part of ready_sg, awaited just
-          // before, except on the last tile, which has no next tile
-          if (!C::GQ_IN_S && t >= 1 && (!C::HELPER || t + 1 >= T)) {
-            if (!warp_wait(gq_empty, (t - 1) & 1, abort_st, prm.status)) return false;
-            tc_fence_after();
-          }
+        // gradQ^T of tile t into its S^T columns, whose A operands the gradK
+        // MMAs above read first (MMAs from one thread run in issue order).
+        // The partial that used them before was drained before this tile's
+        // S^T / G^T were issued.
+        auto issue_gq = [&]() {
           const uint32_t k_m = opaque(k_mn), gk_m = opaque(gk_mn), ds_m = opaque(ds_mn),
                          gs_m = opaque(gs_mn);
 #pragma unroll
           for (int k = 0; k < C::BM / 16; ++k) {  // contraction over the 128 keys
-            mma_ss_w(t_gq, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
-            if (has_gk) mma_ss_w(t_gq, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
+            mma_ss_w(t_s, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
+            if (has_gk) mma_ss_w(t_s, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
           }
           mma_commit_w(gq_full);
-          return true;
         };
         // at d = 128 gradQ^T goes before gradV: its partial is drained sooner,
         // and the next tile's scores wait for that drain
-        if (!C::LATE_GQ && !issue_gq()) { ok = false; break; }
+        if (!C::SG2) issue_gq();
 #pragma unroll
         for (int k = 0; k < C::BN / 16; ++k)
           mma_ts_w(t_gv, t_g + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
         mma_commit_w(do_empty + ds);
-        if (t + 1 < T) {
-          if (C::HELPER && !warp_wait(ready_sg + (t & 1), (t >> 1) & 1, abort_st, prm.status)) {
-            ok = false;
-            break;
-          }
-          if (!issue_sg(t + 1, !C::HELPER)) { ok = false; break; }
+        if (C::SG2) {
+          issue_gq();
+        } else if (t + 1 < T && !next_sg()) {
+          ok = false;
+          break;
         }
-        if (C::LATE_GQ && !issue_gq()) { ok = false; break; }
       }
       if (ok) mma_commit_w(acc_done);
       mma_commit_w(drain);
@@ -923,10 +937,10 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
     const f2 sc2_2 = {sc2, sc2}, scale_2 = {prm.scale, prm.scale};
     const bool has_g = has_gq || has_gk, has_h = has_gv;
     // gradQ^T partial of tile t (TMEM lane = feature index, column = query),
-    // once gq_full(t) has been awaited
-    auto load_gq = [&](uint32_t (&gq)[NC]) {
+    // in the S^T columns of its buffer, once gq_full(t) has been awaited
+    auto load_gq = [&](int t, uint32_t (&gq)[NC]) {
       tc_fence_after();
-      tmem_ld16(tmem + lane_off + C::T_GQ + NC * slice, gq);
+      tmem_ld16(tmem + lane_off + C::T_S(t & 1) + NC * slice, gq);
       tc_fence_before();
       mbar_arrive(gq_empty);  // TMEM region free; the reductions follow
     };
@@ -952,7 +966,8 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
       tc_fence_after();
       uint32_t sr[NC], dpr[NC], gr[NC], hr[NC];
       const uint32_t tl = tmem + lane_off + NC * slice;
-      tmem_ld16x4(tl + C::T_S, tl + C::T_DP, tl + C::T_G, tl + C::T_H, sr, dpr, gr, hr);
+      const uint32_t ts = tl + C::T_S(t & 1), tg = tl + C::T_G(t & 1);
+      tmem_ld16x4(ts, tl + C::T_DP, tg, tl + C::T_H, sr, dpr, gr, hr);
       // the loads above have completed: dP^T, H^T are free
       tc_fence_before();
       mbar_arrive(sc_read);
@@ -1005,11 +1020,11 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
       // query), gS^T and dS^T in the 16 columns this thread read from S^T,
       // gdP^T in the first 8 it read from G^T; one 16-query contraction step
       // per slice
-      tmem_st8x3(tl + C::T_S, gsw, tl + C::T_S + 8, dsw, tl + C::T_G, gdw);
-      // With LATE_GQ the previous tile's gradQ^T MMAs read the dS^T / gS^T
-      // tiles below: wait for them first (their result stays in TMEM until
-      // gq_empty).  Otherwise that wait ended the previous iteration.
-      if (C::LATE_GQ && t >= 1 && !warp_wait(gq_full, (t - 1) & 1, abort_st, prm.status)) {
+      tmem_st8x3(ts, gsw, ts + 8, dsw, tg, gdw);
+      // With SG2 the previous tile's gradQ^T MMAs read the dS^T / gS^T tiles
+      // below: wait for them first.  At d = 128 that wait ended the previous
+      // iteration.
+      if (C::SG2 && t >= 1 && !warp_wait(gq_full, (t - 1) & 1, abort_st, prm.status)) {
         ok = false;
         break;
       }
@@ -1023,26 +1038,32 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
         st_shared_v4(sb + C::OFF_GS + sw128_offset(row, chunk), gsw[4 * q], gsw[4 * q + 1],
                      gsw[4 * q + 2], gsw[4 * q + 3]);
       }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(ds_full);
-      uint32_t gq[NC];
-      if (C::LATE_GQ) {
-        if (t >= 1) {
-          load_gq(gq);
-          reduce_gq(t - 1, gq);
-        }
+      if (C::SG2 && t >= 1) {
+        // drain the previous tile's partial now, which frees the other
+        // buffer for the next tile's scores
+        uint32_t gq[NC];
+        load_gq(t - 1, gq);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+        reduce_gq(t - 1, gq);
       } else {
-        if (!warp_wait(gq_full, t & 1, abort_st, prm.status)) { ok = false; break; }
-        load_gq(gq);
-        reduce_gq(t, gq);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+        if (!C::SG2) {
+          if (!warp_wait(gq_full, t & 1, abort_st, prm.status)) { ok = false; break; }
+          uint32_t gq[NC];
+          load_gq(t, gq);
+          reduce_gq(t, gq);
+        }
       }
     }
-    if (C::LATE_GQ && ok && T >= 1) {
+    if (C::SG2 && ok && T >= 1) {
       ok = warp_wait(gq_full, (T - 1) & 1, abort_st, prm.status);
       if (ok) {
         uint32_t gq[NC];
-        load_gq(gq);
+        load_gq(T - 1, gq);
         reduce_gq(T - 1, gq);
       }
     }
