@@ -548,13 +548,6 @@ struct Col {
                             T_GV = T_GK + D;
   static_assert(T_GV + D == 512, "pass 2 TMEM layout fills 512 columns");
   static constexpr uint32_t TMEM_COLS = 512;
-  // At d = 64 a helper warp folds pairs of the MMA warp's waits into one
-  // barrier each (as in pass 1): (scores read, next dO landed) before the
-  // next tile's dP^T / H^T, and (next [Q|gQ] landed, gradQ^T partial of the
-  // tile before drained) before its S^T / G^T.  At d = 128 the score
-  // read-out and the gradQ^T drain are the last events before the MMAs they
-  // gate, and a hop through another warp adds its wake-up to every tile.
-  static constexpr bool HELPER = SG2;
 };
 
 struct ColParams {
@@ -581,21 +574,20 @@ struct ColParams {
 // warp of its own so that its loads run as far ahead as its ring allows:
 // the next tile's dP^T / H^T MMAs wait for it while the elementwise phase
 // runs, and the [Q|gQ] producer spends most of each tile waiting for the
-// gradK MMAs to free its stage.  Warp 19, at d = 64 only, is the helper
-// (Col::HELPER).
+// gradK MMAs to free its stage.  The MMA warp waits for the elementwise
+// warps itself: these waits gate the next MMAs directly, and folding them
+// through a helper warp (as in pass 1) added a hand-off to every tile.
 constexpr int kColConsumerWarps = 16;
 constexpr int kColConsumers = kColConsumerWarps * 32;
 constexpr int kColProducerWarp = kColConsumerWarps;
 constexpr int kColMmaWarp = kColConsumerWarps + 1;
 constexpr int kColDoWarp = kColConsumerWarps + 2;
-constexpr int kColHelperWarp = kColConsumerWarps + 3;
-template <int D>
-constexpr int col_threads() { return (kColConsumerWarps + (Col<D>::HELPER ? 4 : 3)) * 32; }
+constexpr int kColThreads = (kColConsumerWarps + 3) * 32;
 constexpr int kColCols = 64 / (kColConsumerWarps / 4);  // columns per elementwise thread
 static_assert(kColCols == 16, "one 16-query MMA step per column slice");
 
 template <int D, bool ALL>
-__global__ void __launch_bounds__(col_threads<D>(), 1)
+__global__ void __launch_bounds__(kColThreads, 1)
     bob_col_pass(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mGK,
                  const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mGV,
                  const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mGQ,
@@ -624,9 +616,7 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
   uint64_t* gq_empty = gq_full + 1;
   uint64_t* acc_done = gq_empty + 1;
   uint64_t* drain = acc_done + 1;
-  uint64_t* ready_dh = drain + 1;               // [2] (HELPER): next tile's dP^T / H^T may go
-  uint64_t* ready_sg = ready_dh + 2;            // [2] (HELPER): next tile's S^T / G^T may go
-  static_assert((12 + 2 * C::STAGES + 2 * C::DSTAGES) * 8 <= 256,
+  static_assert((8 + 2 * C::STAGES + 2 * C::DSTAGES) * 8 <= 256,
                 "barriers end below the TMEM slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
   Abort* abort_st = reinterpret_cast<Abort*>(smem + C::OFF_MISC + 264);
@@ -658,12 +648,6 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
     mbar_init(gq_empty, kColConsumers);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
-    if (C::HELPER) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(ready_dh + b, 1);
-        mbar_init(ready_sg + b, 1);
-      }
-    }
     abort_st->flag = 0;
     abort_st->limit_ns = prm.wait_ns;
     fence_mbar_init();
@@ -766,24 +750,6 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
         mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
                           100000000ull);
     }
-  } else if (warp == kColHelperWarp) {
-    if (C::HELPER && lane == 0) {
-      for (int t = 0; t + 1 < T; ++t) {
-        const int u = t + 1;
-        // dP^T / H^T of tile u: tile t's scores read out, dO(u) landed
-        if (!wait_bar(sc_read, t & 1, abort_st, prm.status) ||
-            !wait_bar(do_full + u % C::DSTAGES, (u / C::DSTAGES) & 1, abort_st, prm.status))
-          break;
-        mbar_arrive(ready_dh + (t & 1));
-        // S^T / G^T of tile u: [Q|gQ](u) landed (with its row scalars), and
-        // the gradQ^T partial that the gradQ^T MMAs after them replace (tile
-        // t - 1's) read out
-        if (!wait_bar(qg_full + u % C::STAGES, (u / C::STAGES) & 1, abort_st, prm.status) ||
-            (t >= 1 && !wait_bar(gq_empty, (t - 1) & 1, abort_st, prm.status)))
-          break;
-        mbar_arrive(ready_sg + (t & 1));
-      }
-    }
   } else if (warp == kColMmaWarp) {
     {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
       constexpr uint32_t id_sc = idesc_bf16(128, 64, false, false);  // scores: M=128 N=64
@@ -801,12 +767,11 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
                      t_gv = tmem + C::T_GV;
       // dP^T and H^T of tile t (need dO(t) and the previous tile's scores
       // read out of TMEM)
-      auto issue_dh = [&](int t, bool wait) -> bool {
+      auto issue_dh = [&](int t) -> bool {
         const int ds = t % C::DSTAGES;
         const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
         const uint32_t v_l = opaque(v_lo), gv_l = opaque(gv_lo);
-        if (wait && !warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_st, prm.status))
-          return false;
+        if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_st, prm.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
@@ -822,18 +787,15 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
       // S^T and G^T of tile t into buffer t % 2 (need Q, gQ; overwrite the
       // A operands and the gradQ^T partial of the tile that last used the
       // buffer: t - 1 at d = 128, t - 2 with SG2), then the commit that
-      // covers all four score blocks.  With the helper, wait = false: its
-      // barrier covered both waits.
-      auto issue_sg = [&](int t, bool wait) -> bool {
+      // covers all four score blocks
+      auto issue_sg = [&](int t) -> bool {
         const int s = t % C::STAGES;
         const uint32_t qgq_lo = opaque(lo_kmajor(sb + C::OFF_QG + s * 2 * C::QB));  // [Q;gQ] per half
         const uint32_t k_l = opaque(k_lo), gk_l = opaque(gk_lo);
         const uint32_t t_s = tmem + C::T_S(t & 1), t_g = tmem + C::T_G(t & 1);
         const int prev = C::SG2 ? t - 2 : t - 1;  // the buffer's previous tile
-        if (wait && !warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_st, prm.status))
-          return false;
-        if (wait && prev >= 0 && !warp_wait(gq_empty, prev & 1, abort_st, prm.status))
-          return false;
+        if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_st, prm.status)) return false;
+        if (prev >= 0 && !warp_wait(gq_empty, prev & 1, abort_st, prm.status)) return false;
         tc_fence_after();
         // [S^T | K gQ^T] = K [Q; gQ]^T (S^T = K Q^T alone without gQ), then
         // G^T += gK Q^T (the first BN rows of each [Q;gQ] half are Q)
@@ -852,30 +814,17 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
         mma_commit_w(sc_full);
         return true;
       };
-      // With the helper, loop iteration t waits on phase t >> 1 of
-      // ready_dh[t & 1] and ready_sg[t & 1], the helper's arrivals for tile
-      // t + 1.  Its arrival for tile t + 3 on the same barriers cannot come
-      // before that wait has passed: the helper first needs the scores of
-      // tile t + 2 read out, and S^T(t + 2) is issued by iteration t + 1.
-      bool ok = warp_wait(kv_full, 0, abort_st, prm.status) && issue_dh(0, true) &&
-                issue_sg(0, true);
+      bool ok = warp_wait(kv_full, 0, abort_st, prm.status) && issue_dh(0) && issue_sg(0);
       for (int t = 0; ok && t < T; ++t) {
         const int s = t % C::STAGES, ds = t % C::DSTAGES;
         // ---- next tile's dP^T, H^T while the elementwise warps work ----
         if (t + 1 < T) {
-          const bool w = C::HELPER ? warp_wait(ready_dh + (t & 1), (t >> 1) & 1, abort_st, prm.status)
-                                   : warp_wait(sc_read, t & 1, abort_st, prm.status);
-          if (!w) { ok = false; break; }
+          if (!warp_wait(sc_read, t & 1, abort_st, prm.status)) { ok = false; break; }
           tc_fence_after();
-          if (!issue_dh(t + 1, !C::HELPER)) { ok = false; break; }
+          if (!issue_dh(t + 1)) { ok = false; break; }
         }
         // ---- SG2: next tile's S^T, G^T into the other buffer ----
-        auto next_sg = [&]() -> bool {
-          if (C::HELPER && !warp_wait(ready_sg + (t & 1), (t >> 1) & 1, abort_st, prm.status))
-            return false;
-          return issue_sg(t + 1, !C::HELPER);
-        };
-        if (C::SG2 && t + 1 < T && !next_sg()) { ok = false; break; }
+        if (C::SG2 && t + 1 < T && !issue_sg(t + 1)) { ok = false; break; }
         // ---- outputs: A operands (bf16 gS^T, dS^T, gdP^T) from TMEM ----
         if (!warp_wait(ds_full, t & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
@@ -917,7 +866,7 @@ __global__ void __launch_bounds__(col_threads<D>(), 1)
         mma_commit_w(do_empty + ds);
         if (C::SG2) {
           issue_gq();
-        } else if (t + 1 < T && !next_sg()) {
+        } else if (t + 1 < T && !issue_sg(t + 1)) {
           ok = false;
           break;
         }
@@ -1197,7 +1146,7 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
   cp.has_gk = has_gk;
   cp.has_gv = has_gv;
   dim3 g2((unsigned)(((p.N + Cc::BM - 1) / Cc::BM) * p.BH()));
-  col_kernel<<<g2, col_threads<D>(), Cc::SMEM, log.stream>>>(mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc, cp);
+  col_kernel<<<g2, kColThreads, Cc::SMEM, log.stream>>>(mKc, mGKc, mVc, mGVc, mQc, mGQc, mDOc, cp);
   e = cudaGetLastError();
   log.mark();
   if (e != cudaSuccess) return e;
