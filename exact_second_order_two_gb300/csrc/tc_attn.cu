@@ -432,7 +432,14 @@ struct Bwd {
   static constexpr uint32_t OFF_DO = OFF_Q + STAGES * QB;
   static constexpr uint32_t OFF_DS = OFF_DO + DSTAGES * QB;
   static constexpr uint32_t OFF_SC = OFF_DS + XB;            // [STAGES][2][BN] fp32
-  static constexpr uint32_t OFF_MISC = OFF_SC + STAGES * 2 * BN * 4;
+  // dQ^T partials go from TMEM to global memory through shared memory: the
+  // elementwise warps write a tile's partial as [BN][D] fp32 rows into a
+  // staging buffer and a TMA reduce-add carries it into the accumulator
+  // (one buffer at d = 128, two at d = 64)
+  static constexpr uint32_t STGB = BN * D * 4;
+  static constexpr int SBUF = D == 64 ? 2 : 1;
+  static constexpr uint32_t OFF_STG = (OFF_SC + STAGES * 2 * BN * 4 + 1023) / 1024 * 1024;
+  static constexpr uint32_t OFF_MISC = OFF_STG + SBUF * STGB;
   static constexpr uint32_t MISC = 512;
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "backward shared memory budget");
@@ -455,7 +462,6 @@ struct BwdParams {
   const float* Dv;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* acc;  // fp32 [B,H,N,D] dQ accumulator
   int* status;
   unsigned long long wait_ns;  // limit of one bounded wait
   int N, causal;
@@ -463,18 +469,22 @@ struct BwdParams {
   float scale;
 };
 
+// Warps 0-15 elementwise, 16 TMA producer, 17 MMA issuer, 18 issues the TMA
+// reduce-add of each staged dQ^T partial (per-thread atomics for them kept
+// the elementwise warps issuing for over a thousand cycles per tile).
 constexpr int kBwdConsumerWarps = 16;
 constexpr int kBwdConsumers = kBwdConsumerWarps * 32;
 constexpr int kBwdProducerWarp = kBwdConsumerWarps;
 constexpr int kBwdMmaWarp = kBwdConsumerWarps + 1;
-constexpr int kBwdThreads = (kBwdConsumerWarps + 2) * 32;
+constexpr int kBwdReduceWarp = kBwdConsumerWarps + 2;
+constexpr int kBwdThreads = (kBwdConsumerWarps + 3) * 32;
 constexpr int kBwdCols = 16;  // query columns per elementwise thread
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_col_pass(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                  const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mDO,
-                 BwdParams prm) {
+                 const __grid_constant__ CUtensorMap mACC, BwdParams prm) {
   using C = Bwd<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
@@ -496,7 +506,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* acc_done = dq_empty + 1;
   uint64_t* drain = acc_done + 1;
-  static_assert((11 + 2 * C::STAGES + 2 * C::DSTAGES) * 8 <= 256,
+  uint64_t* stg_full = drain + 1;               // [SBUF]: a dQ^T partial staged
+  uint64_t* stg_free = stg_full + 2;            // [SBUF]: its reduce-add has read it
+  static_assert((15 + 2 * C::STAGES + 2 * C::DSTAGES) * 8 <= 256,
                 "barriers end below the TMEM slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
   Abort* abort_st = reinterpret_cast<Abort*>(smem + C::OFF_MISC + 264);
@@ -530,6 +542,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(dq_empty, kBwdConsumers);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
+    for (int b = 0; b < C::SBUF; ++b) {
+      mbar_init(stg_full + b, kBwdConsumers);
+      mbar_init(stg_free + b, 1);
+    }
     abort_st->flag = 0;
     abort_st->limit_ns = prm.wait_ns;
     fence_mbar_init();
@@ -608,6 +624,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int t = max(0, do_issued - C::DSTAGES); t < do_issued; ++t)
         mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
                           100000000ull);
+    }
+  } else if (warp == kBwdReduceWarp) {
+    if (lane == 0) {
+      // one reduce-add per tile, in tile order: the partial of tile u sits
+      // in staging buffer u % SBUF
+      for (int u = 0; u < T; ++u) {
+        const int b = u % C::SBUF;
+        if (!wait_bar(stg_full + b, (u / C::SBUF) & 1, abort_st, prm.status)) break;
+        tma_reduce_add_3d(&mACC, smem + C::OFF_STG + b * C::STGB, 0,
+                          qstart + rotated(u, rot, T) * C::BN, bh);
+        bulk_commit_group();
+        bulk_wait_read_all();  // the buffer may be refilled
+        mbar_arrive(stg_free + b);
+      }
+      bulk_wait_all();  // every reduce-add has landed before the CTA exits
     }
   } else if (warp == kBwdMmaWarp) {
     {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
@@ -714,17 +745,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(dq_empty);
       return true;
     };
-    auto reduce_dq = [&](int t, const uint32_t (&dq)[NC]) {
-      const int qa = qstart + rotated(t, rot, T) * C::BN + NC * slice;
-      if (D == 128) {
-        red_columns<D, NC>(prm.acc + ((size_t)bh * N + qa) * D + row, dq, N - qa);
-      } else {
-        // M = 64 accumulator: rows 16w' + x (w' = warp & 3, x < 16) live in
-        // lanes 32w' + x; the upper 16 lanes of each warp hold nothing
-        if (lane < 16) {
-          red_columns<D, NC>(prm.acc + ((size_t)bh * N + qa) * D + 16 * (warp & 3) + lane, dq, N - qa);
-        }
+    // dQ^T partial of tile u into staging buffer u % SBUF as [BN][D] fp32
+    // rows (query column c, feature f at c * D + f; a warp's lanes write
+    // consecutive words) once the reduce-add that last used the buffer has
+    // read it, then the arrival that hands it to the reduce warp
+    auto stage_dq = [&](int u, const uint32_t (&dq)[NC]) -> bool {
+      const int b = u % C::SBUF;
+      if (u >= C::SBUF &&
+          !warp_wait(stg_free + b, ((u / C::SBUF) - 1) & 1, abort_st, prm.status))
+        return false;
+      // M = 64 accumulator at d = 64: rows 16w' + x (w' = warp & 3, x < 16)
+      // live in lanes 32w' + x; the upper 16 lanes of each warp hold nothing
+      const int f = D == 128 ? row : 16 * (warp & 3) + lane;
+      if (D == 128 || lane < 16) {
+        const uint32_t base = sb + C::OFF_STG + b * C::STGB + (uint32_t)(NC * slice * D + f) * 4u;
+#pragma unroll
+        for (int i = 0; i < NC; ++i) st_shared_u32(base + (uint32_t)(i * D * 4), dq[i]);
       }
+      fence_async_smem();
+      mbar_arrive(stg_full + b);
+      return true;
     };
     bool ok = true;
     for (int t = 0; t < T; ++t) {
@@ -793,12 +833,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(ds_full);
-      if (t >= 1) reduce_dq(t - 1, dq);
+      if (t >= 1 && !stage_dq(t - 1, dq)) { ok = false; break; }
     }
     if (ok && T >= 1) {
       uint32_t dq[NC];
-      ok = drain_dq(T - 1, dq);
-      if (ok) reduce_dq(T - 1, dq);
+      ok = drain_dq(T - 1, dq) && stage_dq(T - 1, dq);
     }
     // ---- epilogue: dK (scaled), dV; each thread D/4 features ----
     ok = __all_sync(0xffffffffu, ok);
@@ -916,6 +955,8 @@ cudaError_t backward_d(const Problem& p, const void* q, const void* k, const voi
   if (!make_map(&mK, k, p, C::BM) || !make_map(&mV, v, p, C::BM) ||
       !make_map(&mQ, q, p, C::BN) || !make_map(&mDO, dO, p, C::BN))
     return cudaErrorInvalidValue;
+  CUtensorMap mAcc;
+  if (!make_acc_map(&mAcc, ws.acc, p, C::BN)) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(bwd_col_pass<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::SMEM);
   if (e != cudaSuccess) return e;
@@ -924,7 +965,6 @@ cudaError_t backward_d(const Problem& p, const void* q, const void* k, const voi
   bp.Dv = ws.D;
   bp.dk = static_cast<__nv_bfloat16*>(dk);
   bp.dv = static_cast<__nv_bfloat16*>(dv);
-  bp.acc = ws.acc;
   bp.status = ws.status;
   bp.wait_ns = wait_limit_ns();
   bp.N = p.N;
@@ -933,7 +973,7 @@ cudaError_t backward_d(const Problem& p, const void* q, const void* k, const voi
   bp.causal = p.causal;
   bp.scale = p.scale;
   dim3 grid((unsigned)(((p.N + C::BM - 1) / C::BM) * p.BH()));
-  bwd_col_pass<D><<<grid, kBwdThreads, C::SMEM, log.stream>>>(mK, mV, mQ, mDO, bp);
+  bwd_col_pass<D><<<grid, kBwdThreads, C::SMEM, log.stream>>>(mK, mV, mQ, mDO, mAcc, bp);
   e = cudaGetLastError();
   log.mark();
   if (e != cudaSuccess) return e;
