@@ -119,6 +119,45 @@ def test_real_kernels_stop_cleanly_when_their_waits_run_out(d):
         assert err <= 1e-2, err
 
 
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("op", ["forward", "backward"])
+def test_attention_kernels_stop_cleanly_when_their_waits_run_out(op, d):
+    """The same 1 ns wait limit on the forward and on the first backward
+    (whose reduce warp hands dQ^T partials to TMA reduce-adds): the call
+    reports FBOB_ERR_TIMEOUT, and the next call with the default limit
+    matches the one before.  A wait only gives up once the global timer has
+    moved past its limit, and that timer ticks coarsely, so the problem is
+    long enough (16 key tiles per row block) that some wait outlasts a tick."""
+    w = Workload("abort_" + op, 1, 2, 2048, d, "bf16", True, 1.0, 1.0, 0.3)
+    ins = {k: v.cuda() for k, v in make_inputs(w, seed=17).items()}
+    args = (ins["q"], ins["k"], ins["v"])
+    shp = fbob.shape_of(ins["q"], True, w.scale)
+    if op == "forward":
+        ws = fbob.alloc_workspace(fbob.OP_FORWARD, shp, "cuda")
+        call = lambda: fbob.forward(*args, True, w.scale, workspace=ws)
+    else:
+        o, lse = fbob.forward(*args, True, w.scale)
+        ws = fbob.alloc_workspace(fbob.OP_BACKWARD, shp, "cuda")
+        call = lambda: fbob.backward(*args, o, lse, ins["do"], True, w.scale, workspace=ws)
+    ref = [t.clone() for t in call()]
+    assert fbob.status(ws) == 0
+    old = fbob.set_wait_limit(1)
+    try:
+        call()
+        st = fbob.status(ws)
+    finally:
+        fbob.set_wait_limit(old)
+    assert st == 5  # FBOB_ERR_TIMEOUT
+    got = call()
+    assert fbob.status(ws) == 0
+    torch.cuda.synchronize()
+    # dQ sums partials from many blocks in no fixed order: compare with a
+    # tolerance rather than bit for bit
+    for g, r in zip(got, ref):
+        err = ((g.double() - r.double()).abs().max() / r.double().abs().max()).item()
+        assert err <= 1e-2, err
+
+
 def test_launch_count_is_reported():
     w = Workload("count", 1, 1, 128, 64, "bf16", True, 1.0, 1.0, 0.2)
     ins = {k: v.cuda() for k, v in make_inputs(w, seed=3).items()}
