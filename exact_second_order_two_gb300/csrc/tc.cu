@@ -58,7 +58,8 @@ constexpr int kMmaWarp = 9;
 // pipe streams its operands, and the pipe holds only a few MMAs of work to
 // cover it, so one wait per tile leaves it idle far less than three.
 constexpr int kHelperWarp = 10;
-constexpr int kThreads = 352;
+// At d = 64 a second MMA warp takes the odd tiles (Row::TWO_MMA).
+constexpr int kMmaWarp2 = 11;
 constexpr int kConsumers = kConsumerWarps * 32;
 __device__ __forceinline__ void consumer_sync() { named_sync<kConsumers>(1); }
 
@@ -111,7 +112,16 @@ struct Row {
   // bf16 P (or P*G) of keys [16k, 16k + 16): column offset in the S (G) block
   __host__ __device__ static constexpr uint32_t p_col(int k) { return 32u * (k >> 1) + 8u * (k & 1); }
   static constexpr uint32_t T_QA = 256 + D, T_GQA = 256 + D + D / 2;
-  static_assert(T_GQA + D / 2 <= TMEM_COLS, "pass 1 TMEM budget");
+  // d = 64: two MMA warps, one per tile parity, each with its own W
+  // accumulator (summed in the epilogue).  Every MMA warp stalls for a few
+  // hundred cycles after each tile's burst of MMAs; with two, one warp's
+  // stall is covered by the other's burst.  Buffer t % 2 and ready[t % 2]
+  // already belong to one parity, so the warps share nothing else that
+  // needs ordering.  At d = 128 TMEM has no room for a second W.
+  static constexpr bool TWO_MMA = D == 64;
+  static constexpr uint32_t T_W2 = T_GQA + D / 2;
+  static_assert(T_GQA + D / 2 + (TWO_MMA ? D : 0) <= TMEM_COLS, "pass 1 TMEM budget");
+  static constexpr int THREADS = (TWO_MMA ? 12 : 11) * 32;
 };
 
 struct RowParams {
@@ -134,7 +144,7 @@ struct RowParams {
 };
 
 template <int D, bool ALL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Row<D>::THREADS, 1)
     bob_row_pass(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mGQ,
                  const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mGK,
                  const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mGV,
@@ -162,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_tmem = w_done + 2;                  // Q, gQ copied into TMEM
   uint64_t* drain = w_done + 1;
   uint64_t* ready = q_tmem + 1;                   // [2]: P(t), V(t), K(t+2) all in place
-  static_assert((1 + 2 * C::STAGES + 2 * C::VSTAGES + 9) * 8 <= 256,
+  uint64_t* drain2 = ready + 2;                   // TWO_MMA: the second MMA warp's drain
+  static_assert((1 + 2 * C::STAGES + 2 * C::VSTAGES + 10) * 8 <= 256,
                 "barriers end below the TMEM slot");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
   Abort* abort_st = reinterpret_cast<Abort*>(smem + C::OFF_MISC + 264);
@@ -194,8 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sg_full + b, 1);
       mbar_init(p_full + b, kConsumers);
     }
-    mbar_init(w_done, 1);
+    mbar_init(w_done, C::TWO_MMA ? 2 : 1);
     mbar_init(drain, 1);
+    mbar_init(drain2, 1);
     mbar_init(q_tmem, kConsumers);
     mbar_init(ready, 1);
     mbar_init(ready + 1, 1);
@@ -263,13 +275,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(v_full + (t % C::VSTAGES), (t / C::VSTAGES) & 1, prm.status,
                           100000000ull);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || (C::TWO_MMA && warp == kMmaWarp2)) {
     {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
+      // tiles par, par + step, ...: all of them, or (TWO_MMA) one parity
+      const int par = warp == kMmaWarp ? 0 : 1, step = C::TWO_MMA ? 2 : 1;
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);    // gQ K^T: M=128 N=64
       constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // Q [K;gK]^T: N=128
       constexpr uint32_t id_w = idesc_bf16(128, D, false, true);    // W: N=D, B MN-major
       bool ok = warp_wait(q_tmem, 0, abort_st, prm.status);
-      const uint32_t tw = tmem + C::T_W, tq = tmem + C::T_QA, tgq = tmem + C::T_GQA;
+      const uint32_t tw = tmem + (par == 0 ? C::T_W : C::T_W2), tq = tmem + C::T_QA,
+                     tgq = tmem + C::T_GQA;
       // S and G of tile t into buffer t & 1
       auto wait_sg = [&](int t) -> bool {
         return warp_wait(kg_full + t % C::STAGES, (t / C::STAGES) & 1, abort_st, prm.status);
@@ -302,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t v_lo = opaque(lo_mnmajor(st, C::BN * 128)),
                        gv_lo = opaque(lo_mnmajor(st + C::KB, C::BN * 128));
         const uint32_t tp = tmem + C::T_S(b), tpg = tmem + C::T_G(b);
-        const uint32_t first = t > 0 ? 1u : 0u;
+        const uint32_t first = t >= step ? 1u : 0u;  // this warp's first tile starts its W
         // without gV only (P*G) V; without gQ and gK, G = 0 and only P gV
         const bool use_gv = has_gv, use_g = has_gq || has_gk;
 #pragma unroll
@@ -316,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Buffer b holds tile t until the W MMAs of t have read its P: the S/G
       // MMAs of tile t + 2 are issued after them, and MMAs from one thread
       // run in issue order.
-      for (int t = 0; ok && t < 2 && t < T; ++t) {
+      for (int t = par; ok && t < 2 && t < T; t += step) {
         ok = wait_sg(t);
         if (ok) {
           tc_fence_after();
@@ -327,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // phase of ready[t & 1] cannot be signalled before the MMA warp has
       // passed its wait for tile t - 2: the helper first needs P(t), which
       // needs S(t), issued only after that wait.
-      for (int t = 0; ok && t < T; ++t) {
+      for (int t = par; ok && t < T; t += step) {
         if (!warp_wait(ready + (t & 1), (t >> 1) & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
         issue_w(t);
@@ -335,8 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) mma_commit_w(w_done);
       // every MMA this thread issued has completed before TMEM is released
-      mma_commit_w(drain);
-      mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
+      uint64_t* dr = par == 0 ? drain : drain2;
+      mma_commit_w(dr);
+      mbar_wait_bounded(dr, 0, prm.status, 100000000ull);
     }
   } else if (warp == kHelperWarp) {
     if (lane == 0) {
@@ -447,6 +463,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cc = 0; cc < HALF; cc += 32) {
         uint32_t wr[32];
         tmem_ld32(tmem + lane_off + C::T_W + HALF * half + cc, wr);
+        if (C::TWO_MMA && T >= 2) {  // the odd tiles' share, from the second MMA warp
+          uint32_t w2[32];
+          tmem_ld32(tmem + lane_off + C::T_W2 + HALF * half + cc, w2);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            wr[e] = __float_as_uint(__uint_as_float(wr[e]) + __uint_as_float(w2[e]));
+        }
         if (row_ok) {
           const uint4* op = reinterpret_cast<const uint4*>(prm.o + obase + cc);
           const uint4* dp = reinterpret_cast<const uint4*>(prm.dO + obase + cc);
@@ -1122,7 +1145,7 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
   rp.has_gk = has_gk;
   rp.has_gv = has_gv;
   dim3 g1((unsigned)(((p.N + R::BM - 1) / R::BM) * p.BH()));
-  row_kernel<<<g1, kThreads, R::SMEM, log.stream>>>(mQr, mGQr, mKr, mGKr, mVr, mGVr, rp);
+  row_kernel<<<g1, R::THREADS, R::SMEM, log.stream>>>(mQr, mGQr, mKr, mGKr, mVr, mGVr, rp);
   e = cudaGetLastError();
   log.mark();
   if (e != cudaSuccess) return e;
