@@ -15,21 +15,25 @@
 //   pass 1 (row-stationary, 128 query rows per CTA, 64-key tiles streamed):
 //     S and G on the tensor cores into one of two TMEM buffers; P and P*G in
 //     registers, written back as bf16 into the S / G columns just read;
-//     W += P gV + (P*G) V into TMEM with those as A operands; epilogue r, D,
+//     W += P gV + (P*G) V into TMEM with those as A operands (at d = 64 two
+//     MMA warps take alternate tiles, each into its own W); epilogue r, D,
 //     sigma, graddO = W - r O.
 //   pass 2 (key-stationary, 128 key rows per CTA, 64-query tiles streamed):
 //     S^T, dP^T, G^T, H^T into TMEM; dS^T, gdP^T, gS^T in registers, written
 //     back as bf16 into TMEM (A operands of gradV += gdP^T dO and gradK +=
 //     gS^T Q + dS^T gQ) and dS^T, gS^T also into shared memory (B operands
 //     of the gradQ^T partial K^T gS^T + gK^T dS^T, reduced into an fp32
-//     accumulator with red.global.add).
+//     accumulator with red.global.add).  At d = 64 TMEM holds two S^T / G^T
+//     buffers, so the next tile's scores run during this tile's
+//     elementwise phase.
 //   convert: fp32 gradQ accumulator -> bf16.
 //
 // No N x N tensor ever leaves TMEM / shared memory / registers.  Warp roles
-// per CTA: elementwise warps (thread = TMEM lane), a TMA producer warp (one
-// issuing thread), and one warp that allocates TMEM and issues every
-// tcgen05.mma with all its lanes (elect.sync picks the issuing lane).  Every
-// wait is bounded (see common.cuh).
+// per CTA: elementwise warps (thread = TMEM lane), TMA producer warps (one
+// issuing thread each), a warp that allocates TMEM and issues tcgen05.mma
+// with all its lanes (elect.sync picks the issuing lane), and in pass 1 a
+// helper warp that folds the MMA warp's waits.  Every wait is bounded (see
+// common.cuh).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -15,13 +15,15 @@
 // first backward (key-stationary, 128 key rows per CTA, 64-query tiles):
 //   S^T and dP^T into TMEM; bf16 P^T and dS^T written back into the S^T
 //   columns as the A operands of dV += P^T dO and dK += dS^T Q; the next
-//   tile's scores are issued before this tile's dQ^T = K^T dS^T, which is
-//   reduced into an fp32 accumulator one tile late, then converted.
+//   tile's scores are issued before this tile's dQ^T = K^T dS^T, which the
+//   elementwise warps read out one tile late and stage in shared memory; a
+//   TMA reduce-add carries it into an fp32 accumulator, then converted.
 //
 // Warp roles as in the BoB kernels: elementwise warps own TMEM lanes, one TMA
 // producer warp, one MMA warp (TMEM allocator; elect.sync picks the issuing
-// lane).  Every mbarrier wait is bounded, and every warp-collective operation
-// sits in warp-uniform control flow.
+// lane), and in the first backward a warp issuing the reduce-adds.  Every
+// mbarrier wait is bounded, and every warp-collective operation sits in
+// warp-uniform control flow.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
