@@ -193,7 +193,11 @@ __global__ void __launch_bounds__(Row<D>::THREADS, 1)
   const int i0 = blk * C::BM;
   const int kend = prm.causal ? min(N, i0 + C::BM) : N;
   const int T = (kend + C::BN - 1) / C::BN;
-  const int rot = blk % T;  // start tile of this CTA's key loop
+  // Every CTA walks the key tiles from the first: the CTAs of one head then
+  // read the same K / V tiles at about the same time and share them in L2.
+  // (Pass 2 starts each CTA at a different query tile instead; there that
+  // measured faster at long N, here slower.)
+  const int rot = 0;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
