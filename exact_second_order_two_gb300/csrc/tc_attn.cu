@@ -137,7 +137,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int i0 = blk * C::BM;
   const int kend = prm.causal ? min(N, i0 + C::BM) : N;
   const int T = (kend + C::BN - 1) / C::BN;
-  const int rot = blk % T;
+  // every CTA walks the key tiles from the first, so the CTAs of one head
+  // share them in L2 (as in BoB pass 1)
+  const int rot = 0;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -523,7 +525,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int j0 = cc.blk * C::BM;
   const int qstart = prm.causal ? (j0 / C::BN) * C::BN : 0;
   const int T = (N - qstart + C::BN - 1) / C::BN;
-  const int rot = cc.blk % T;
+  // every CTA walks the query tiles from its first (unlike BoB pass 2,
+  // where rotated start tiles measured faster at long N)
+  const int rot = 0;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
