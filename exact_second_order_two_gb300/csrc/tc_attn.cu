@@ -699,6 +699,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (!warp_wait(ds_full, t & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
+        // dQ^T of tile t first, once the previous one has been read out of
+        // TMEM: the next tile's elementwise phase drains it, and issued
+        // before dK / dV it is ready sooner (dK / dV only free ring stages
+        // and this tile's S^T buffer, which are not needed yet)
+        if (t >= 1) {
+          if (!warp_wait(dq_empty, (t - 1) & 1, abort_st, prm.status)) { ok = false; break; }
+          tc_fence_after();
+        }
+        {
+          const uint32_t k_m = opaque(k_mn), ds_m = opaque(ds_mn);
+#pragma unroll
+          for (int k = 0; k < C::BM / 16; ++k)  // contraction over the 128 keys
+            mma_ss_w(t_dq, k_m + kstep_off(k), ds_m + kstep_off(k), id_dq, k > 0 ? 1u : 0u);
+          mma_commit_w(dq_full);
+        }
         {
           const uint32_t q_mn = opaque(lo_mnmajor(sb + C::OFF_Q + s * C::QB, C::BN * 128));
           const uint32_t do_mn = opaque(lo_mnmajor(sb + C::OFF_DO + ds * C::QB, C::BN * 128));
@@ -713,19 +728,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int k = 0; k < C::BN / 16; ++k)
             mma_ts_w(t_dv, t_s + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
           mma_commit_w(do_empty + ds);
-        }
-        // dQ^T of tile t, once the previous one has been read out of TMEM;
-        // it runs during the next tile's elementwise phase, which drains it
-        if (t >= 1) {
-          if (!warp_wait(dq_empty, (t - 1) & 1, abort_st, prm.status)) { ok = false; break; }
-          tc_fence_after();
-        }
-        {
-          const uint32_t k_m = opaque(k_mn), ds_m = opaque(ds_mn);
-#pragma unroll
-          for (int k = 0; k < C::BM / 16; ++k)  // contraction over the 128 keys
-            mma_ss_w(t_dq, k_m + kstep_off(k), ds_m + kstep_off(k), id_dq, k > 0 ? 1u : 0u);
-          mma_commit_w(dq_full);
         }
       }
       if (ok) mma_commit_w(acc_done);
