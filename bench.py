@@ -342,6 +342,10 @@ def run_ours(args, w, rank, world, dist):
         "dtype": w.dtype if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": workload_config(w),
         "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+        # the same time counted with the 12 products a schedule without
+        # recomputation would run (pass 2 recomputes S and G)
+        "f_min": {"value": world * flops_bob(w, 12) / (ms * 1e-3) / 1e12, "unit": UNIT,
+                  "formula": "24*B*H*N^2*d" + ("/2 (causal)" if w.causal else "")},
         "kernel_family": "tcgen05" if kpath == 1 else "simt",
         "kernels_ms": {n: t for n, _, t in per_kernel},
         "roofline": {"bound": "tensor", "kernel": dom[0], "achieved": achieved, "peak": peak,

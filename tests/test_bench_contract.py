@@ -43,6 +43,8 @@ def test_flop_formula():
     assert abs(bench.flops_bob(w) - 30 * 2 * 16 * 16384 ** 2 * 128 / 2) < 1.0
     nc = WORKLOADS["fp32_n256_d64"]
     assert bench.flops_bob(nc) == 30 * 256 ** 2 * 64
+    # F_min: the 12 products of a schedule without recomputation
+    assert bench.flops_bob(w, 12) == 24 * 2 * 16 * 16384 ** 2 * 128 / 2
 
 
 def test_warmup_below_three_is_refused():
