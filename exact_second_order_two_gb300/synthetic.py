@@ -68,6 +68,12 @@ WORKLOADS = {
                  1.0, 1.0, 0.1),
         Workload("bf16_h4_n262144_d64", 1, 4, 262144, 64, "bf16", False,
                  1.0, 1.0, 0.1),
+        # B*H = 3 with 256 blocks per head: the kernels take heads in groups
+        # of two, so the last group is partial
+        Workload("bf16_causal_b3_n32768_d128", 3, 1, 32768, 128, "bf16", True,
+                 1.0, 1.0, 0.1),
+        Workload("bf16_causal_b3_n32768_d64", 3, 1, 32768, 64, "bf16", True,
+                 1.0, 1.0, 0.1),
         # profiling-sized cases (inputs still larger than L2 in total)
         Workload("bf16_causal_h8_n8192_d128", 1, 8, 8192, 128, "bf16", True,
                  1.0, 1.0, 0.1),

@@ -133,6 +133,10 @@ FULL_SIZE_SAMPLES = {
     # no mask: every query sees every key, so one block (across the key
     # block boundary at 8192) costs a full head
     "bf16_h4_n16384_d128": (16, [(0, 2, 8192 - 32, 64)], 0),
+    # B*H = 3 at N = 32768: heads taken in groups of two, the last group
+    # holding one head; every head is sampled
+    "bf16_causal_b3_n32768_d128": (12, [(b, 0, 32768 - 1088, 64) for b in range(3)], 32),
+    "bf16_causal_b3_n32768_d64": (12, [(b, 0, 32768 - 1088, 64) for b in range(3)], 32),
 }
 
 

@@ -177,6 +177,19 @@ def test_noncausal_n16384_d128_sampled():
     sampled_check(WORKLOADS["bf16_h4_n16384_d128"])
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("d", [128, 64])
+def test_partial_last_head_group(d):
+    """The tensor-core kernels visit (batch, head) units in groups of G heads
+    (the smallest power of two giving two waves of CTAs per group).  With
+    B*H = 3 and 256 row / key blocks per head, G = 2, so the last group holds
+    a single head, which takes the partial-group branch of the CTA
+    numbering.  Every head is compared with the oracle (sampled rows, the
+    last key columns, and an earlier key block of the lone head), and the
+    invariants hold on the full outputs."""
+    sampled_check(WORKLOADS[f"bf16_causal_b3_n32768_d{d}"], seed=5)
+
+
 def rows_check(w: Workload, heads, n_rows=12, seed=0):
     """Sampled query rows of a few heads against the oracle, and the exact
     invariants on the full outputs.  Without the mask every key column's
