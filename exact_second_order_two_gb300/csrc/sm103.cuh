@@ -397,6 +397,22 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
 
 // 2^x with the hardware approximation (PTX ex2.approx.ftz.f32); inputs are
 // scores minus the row log-sum-exp, so results lie in [0, 1] up to rounding.
+// Warpgroup register reallocation (PTX ISA: setmaxnreg).  Every thread of
+// a warpgroup (four consecutive warps) must execute the same instruction.
+// A release returns registers to the CTA's pool; a claim waits until the
+// pool holds enough, so the claims of all warpgroups must fit in what the
+// CTA launched with (threads x registers per thread).
+template <int N>
+__device__ __forceinline__ void regs_release() {
+  static_assert(N >= 24 && N <= 256 && N % 8 == 0, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void regs_claim() {
+  static_assert(N >= 24 && N <= 256 && N % 8 == 0, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

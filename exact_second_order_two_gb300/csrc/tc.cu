@@ -579,6 +579,16 @@ struct Col {
                             T_GV = T_GK + D;
   static_assert(T_GV + D == 512, "pass 2 TMEM layout fills 512 columns");
   static constexpr uint32_t TMEM_COLS = 512;
+  // Registers per thread after the split: 640 threads launch with 96 each
+  // (five warps share each SM sub-partition's 64 KB register file), and the
+  // control warpgroup gives the elementwise warps its surplus.  More would
+  // overdraw the launch's registers, and a claim that cannot be met waits
+  // forever, so the host checks the kernel's register count first.  The
+  // elementwise phase at 96 spills and is latency-bound: 104 removes the
+  // d = 128 spills (pass 2 9.36 -> 8.93 ms at the benchmark workload).  The
+  // control split differs per d only because ptxas spills less that way.
+  static constexpr int REGS_ELEMENTWISE = 104, REGS_CONTROL = D == 128 ? 56 : 64;
+  static constexpr int REGS_NEEDED = 16 * 32 * REGS_ELEMENTWISE + 4 * 32 * REGS_CONTROL;
 };
 
 struct ColParams {
@@ -608,12 +618,14 @@ struct ColParams {
 // gradK MMAs to free its stage.  The MMA warp waits for the elementwise
 // warps itself: these waits gate the next MMAs directly, and folding them
 // through a helper warp (as in pass 1) added a hand-off to every tile.
+// Warp 19 has no role: it completes warps 16-19 to a warpgroup, the unit in
+// which setmaxnreg moves registers (see Col::REGS_*).
 constexpr int kColConsumerWarps = 16;
 constexpr int kColConsumers = kColConsumerWarps * 32;
 constexpr int kColProducerWarp = kColConsumerWarps;
 constexpr int kColMmaWarp = kColConsumerWarps + 1;
 constexpr int kColDoWarp = kColConsumerWarps + 2;
-constexpr int kColThreads = (kColConsumerWarps + 3) * 32;
+constexpr int kColThreads = (kColConsumerWarps + 4) * 32;
 constexpr int kColCols = 64 / (kColConsumerWarps / 4);  // columns per elementwise thread
 static_assert(kColCols == 16, "one 16-query MMA step per column slice");
 
@@ -692,221 +704,228 @@ __global__ void __launch_bounds__(kColThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kColProducerWarp) {
-    if (lane == 0) {
-      mbar_arrive_expect_tx(kv_full, (2 + (has_gk ? 1 : 0) + (has_gv ? 1 : 0)) * C::KB);
-      load_tile(smem + C::OFF_K, &mK, kv_full, j0, bh);
-      if (has_gk) load_tile(smem + C::OFF_GK, &mGK, kv_full, j0, bh);
-      load_tile(smem + C::OFF_V, &mV, kv_full, j0, bh);
-      if (has_gv) load_tile(smem + C::OFF_GV, &mGV, kv_full, j0, bh);
-    }
-    bool ok = true;
-    // row scalars (lse pre-scaled by log2 e, D, r, sigma) of the next query
-    // tile are fetched into registers one tile ahead, off the critical path
-    constexpr int PER = C::BN / 32;
-    float pre[4][PER];
-    auto fetch = [&](int q0) {
-#pragma unroll
-      for (int u = 0; u < PER; ++u) {
-        const int q = q0 + lane + 32 * u;
-        const bool in = q < N;
-        const size_t idx = (size_t)bh * N + (in ? q : 0);
-        pre[0][u] = in ? prm.lse[idx] * kLog2e : 0.f;
-        pre[1][u] = in ? prm.Dv[idx] : 0.f;
-        pre[2][u] = in ? prm.r[idx] : 0.f;
-        pre[3][u] = in ? prm.sigma[idx] : 0.f;
-      }
-    };
-    fetch(qstart + rotated(0, rot, T) * C::BN);
-    int qg_issued = 0;
-    for (int t = 0; t < T; ++t) {
-      const int s = t % C::STAGES;
-      const int q0 = qstart + rotated(t, rot, T) * C::BN;
-      const int q_next = qstart + rotated(t + 1 < T ? t + 1 : 0, rot, T) * C::BN;
-      // Row scalars of tile t, stored negated (every one of them is
-      // subtracted).  Their buffer was last read by the elementwise warps of
-      // tile t - SCSTAGES, which finished before that tile's gradK MMAs
-      // released its [Q|gQ] stage, awaited in the previous iteration.
-      float* sc = scal + (t % C::SCSTAGES) * 4 * C::BN;
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = -pre[a][u];
-      __syncwarp();
-      // the next tile's scalars are in flight while this warp waits below
-      if (t + 1 < T) fetch(q_next);
-      bool w = true;
-      if (lane == 0 && t >= C::STAGES)
-        w = wait_bar(qg_empty + s, ((t / C::STAGES) - 1) & 1, abort_st, prm.status);
-      ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-      if (!ok) break;
+  if (warp >= kColConsumerWarps) {
+    // control warpgroup (warps 16-19): it hands registers to the
+    // elementwise warpgroups as one, then splits into its roles; warp 19
+    // only completes the warpgroup
+    regs_release<C::REGS_CONTROL>();
+    if (warp == kColProducerWarp) {
       if (lane == 0) {
-        // this arrival publishes the scalars written above with the stage
-        mbar_arrive_expect_tx(qg_full + s, (has_gq ? 2 : 1) * C::QB);
-        load_pair_opt<D>(smem + C::OFF_QG + s * 2 * C::QB, &mQ, &mGQ, has_gq, qg_full + s,
-                         C::BN, q0, bh);
-        ++qg_issued;
-        if (t + 1 < T) {  // warm L2 with the next query tile
-          tma_prefetch_l2_4d(&mQ, 0, q_next, 0, bh);
-          if (has_gq) tma_prefetch_l2_4d(&mGQ, 0, q_next, 0, bh);
-        }
+        mbar_arrive_expect_tx(kv_full, (2 + (has_gk ? 1 : 0) + (has_gv ? 1 : 0)) * C::KB);
+        load_tile(smem + C::OFF_K, &mK, kv_full, j0, bh);
+        if (has_gk) load_tile(smem + C::OFF_GK, &mGK, kv_full, j0, bh);
+        load_tile(smem + C::OFF_V, &mV, kv_full, j0, bh);
+        if (has_gv) load_tile(smem + C::OFF_GV, &mGV, kv_full, j0, bh);
       }
-    }
-    // every load this warp issued has landed before the CTA exits (after an
-    // abort some were never awaited); each phase waited for is the last of
-    // its barrier, so on the normal path these return at once
-    if (lane == 0) {
-      mbar_wait_bounded(kv_full, 0, prm.status, 100000000ull);
-      for (int t = max(0, qg_issued - C::STAGES); t < qg_issued; ++t)
-        mbar_wait_bounded(qg_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
-                          100000000ull);
-    }
-  } else if (warp == kColDoWarp) {
-    if (lane == 0) {
-      int do_issued = 0;
+      bool ok = true;
+      // row scalars (lse pre-scaled by log2 e, D, r, sigma) of the next query
+      // tile are fetched into registers one tile ahead, off the critical path
+      constexpr int PER = C::BN / 32;
+      float pre[4][PER];
+      auto fetch = [&](int q0) {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const int q = q0 + lane + 32 * u;
+          const bool in = q < N;
+          const size_t idx = (size_t)bh * N + (in ? q : 0);
+          pre[0][u] = in ? prm.lse[idx] * kLog2e : 0.f;
+          pre[1][u] = in ? prm.Dv[idx] : 0.f;
+          pre[2][u] = in ? prm.r[idx] : 0.f;
+          pre[3][u] = in ? prm.sigma[idx] : 0.f;
+        }
+      };
+      fetch(qstart + rotated(0, rot, T) * C::BN);
+      int qg_issued = 0;
       for (int t = 0; t < T; ++t) {
-        const int ds = t % C::DSTAGES;
-        if (t >= C::DSTAGES &&
-            !wait_bar(do_empty + ds, ((t / C::DSTAGES) - 1) & 1, abort_st, prm.status))
-          break;
-        mbar_arrive_expect_tx(do_full + ds, C::QB);
-        load_tile(smem + C::OFF_DO + ds * C::QB, &mDO, do_full + ds,
-                  qstart + rotated(t, rot, T) * C::BN, bh);
-        ++do_issued;
-        if (t + 1 < T)  // warm L2 with the next dO tile
-          tma_prefetch_l2_4d(&mDO, 0, qstart + rotated(t + 1, rot, T) * C::BN, 0, bh);
-      }
-      // every load this thread issued has landed before the CTA exits
-      for (int t = max(0, do_issued - C::DSTAGES); t < do_issued; ++t)
-        mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
-                          100000000ull);
-    }
-  } else if (warp == kColMmaWarp) {
-    {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
-      constexpr uint32_t id_sc = idesc_bf16(128, 64, false, false);  // scores: M=128 N=64
-      constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // K [Q;gQ]^T: N=128
-      constexpr uint32_t id_out = idesc_bf16(128, D, false, true);   // gradK/V: N=D, B MN
-      constexpr uint32_t id_gq = idesc_bf16(D, 64, true, true);      // gradQ^T: M=D, A,B MN
-      // descriptor low words of the stationary tiles: K-major for the score
-      // MMAs, MN-major (64-feature groups BM*128 bytes apart) for gradQ^T
-      const uint32_t k_lo = lo_kmajor(sb + C::OFF_K), gk_lo = lo_kmajor(sb + C::OFF_GK),
-                     v_lo = lo_kmajor(sb + C::OFF_V), gv_lo = lo_kmajor(sb + C::OFF_GV);
-      const uint32_t k_mn = lo_mnmajor(sb + C::OFF_K, C::BM * 128),
-                     gk_mn = lo_mnmajor(sb + C::OFF_GK, C::BM * 128);
-      const uint32_t ds_mn = lo_mnmajor(sb + C::OFF_DS, 1024), gs_mn = lo_mnmajor(sb + C::OFF_GS, 1024);
-      const uint32_t t_dp = tmem + C::T_DP, t_h = tmem + C::T_H, t_gk = tmem + C::T_GK,
-                     t_gv = tmem + C::T_GV;
-      // dP^T and H^T of tile t (need dO(t) and the previous tile's scores
-      // read out of TMEM)
-      auto issue_dh = [&](int t) -> bool {
-        const int ds = t % C::DSTAGES;
-        const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
-        const uint32_t v_l = opaque(v_lo), gv_l = opaque(gv_lo);
-        if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_st, prm.status)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ss_w(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc, k > 0 ? 1u : 0u);
-        if (has_gv) {
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(t_h, gv_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
-                   k > 0 ? 1u : 0u);
-        }
-        return true;
-      };
-      // S^T and G^T of tile t into buffer t % 2 (need Q, gQ; overwrite the
-      // A operands and the gradQ^T partial of the tile that last used the
-      // buffer: t - 1 at d = 128, t - 2 with SG2), then the commit that
-      // covers all four score blocks
-      auto issue_sg = [&](int t) -> bool {
         const int s = t % C::STAGES;
-        const uint32_t qgq_lo = opaque(lo_kmajor(sb + C::OFF_QG + s * 2 * C::QB));  // [Q;gQ] per half
-        const uint32_t k_l = opaque(k_lo), gk_l = opaque(gk_lo);
-        const uint32_t t_s = tmem + C::T_S(t & 1), t_g = tmem + C::T_G(t & 1);
-        const int prev = C::SG2 ? t - 2 : t - 1;  // the buffer's previous tile
-        if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_st, prm.status)) return false;
-        if (prev >= 0 && !warp_wait(gq_empty, prev & 1, abort_st, prm.status)) return false;
-        tc_fence_after();
-        // [S^T | K gQ^T] = K [Q; gQ]^T (S^T = K Q^T alone without gQ), then
-        // G^T += gK Q^T (the first BN rows of each [Q;gQ] half are Q)
-        const uint32_t id_first = has_gq ? id_sg : id_sc;
+        const int q0 = qstart + rotated(t, rot, T) * C::BN;
+        const int q_next = qstart + rotated(t + 1 < T ? t + 1 : 0, rot, T) * C::BN;
+        // Row scalars of tile t, stored negated (every one of them is
+        // subtracted).  Their buffer was last read by the elementwise warps of
+        // tile t - SCSTAGES, which finished before that tile's gradK MMAs
+        // released its [Q|gQ] stage, awaited in the previous iteration.
+        float* sc = scal + (t % C::SCSTAGES) * 4 * C::BN;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ss_w(t_s, k_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_first,
-                 k > 0 ? 1u : 0u);
-        if (has_gk) {
-          const uint32_t g0 = has_gq ? 1u : 0u;  // without gQ this starts G^T
+        for (int a = 0; a < 4; ++a)
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_w(t_g, gk_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_sc,
-                   k > 0 ? 1u : g0);
-        }
-        mma_commit_w(sc_full);
-        return true;
-      };
-      bool ok = warp_wait(kv_full, 0, abort_st, prm.status) && issue_dh(0) && issue_sg(0);
-      for (int t = 0; ok && t < T; ++t) {
-        const int s = t % C::STAGES, ds = t % C::DSTAGES;
-        // ---- next tile's dP^T, H^T while the elementwise warps work ----
-        if (t + 1 < T) {
-          if (!warp_wait(sc_read, t & 1, abort_st, prm.status)) { ok = false; break; }
-          tc_fence_after();
-          if (!issue_dh(t + 1)) { ok = false; break; }
-        }
-        // ---- SG2: next tile's S^T, G^T into the other buffer ----
-        if (C::SG2 && t + 1 < T && !issue_sg(t + 1)) { ok = false; break; }
-        // ---- outputs: A operands (bf16 gS^T, dS^T, gdP^T) from TMEM ----
-        if (!warp_wait(ds_full, t & 1, abort_st, prm.status)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t t_s = tmem + C::T_S(t & 1), t_g = tmem + C::T_G(t & 1);
-        const uint32_t qgq_s = sb + C::OFF_QG + s * 2 * C::QB;
-        // B operands MN-major: 64-feature groups 2*BN*128 bytes apart in the
-        // interleaved [Q;gQ] stage, BN*128 apart in the dO tile
-        const uint32_t q_mn = opaque(lo_mnmajor(qgq_s, 2 * C::BN * 128)),
-                       gq_mn = opaque(lo_mnmajor(qgq_s + C::BN * 128, 2 * C::BN * 128));
-        const uint32_t do_mn = opaque(lo_mnmajor(sb + C::OFF_DO + ds * C::QB, C::BN * 128));
-        const uint32_t first = t > 0 ? 1u : 0u;
-        // gradK first: it releases the [Q|gQ] stage that the next tile waits for
-#pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 queries
-          mma_ts_w(t_gk, t_s + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-          if (has_gq) mma_ts_w(t_gk, t_s + 16 * k + 8, gq_mn + kstep_off(k), id_out, 1u);
-        }
-        mma_commit_w(qg_empty + s);
-        // gradQ^T of tile t into its S^T columns, whose A operands the gradK
-        // MMAs above read first (MMAs from one thread run in issue order).
-        // The partial that used them before was drained before this tile's
-        // S^T / G^T were issued.
-        auto issue_gq = [&]() {
-          const uint32_t k_m = opaque(k_mn), gk_m = opaque(gk_mn), ds_m = opaque(ds_mn),
-                         gs_m = opaque(gs_mn);
-#pragma unroll
-          for (int k = 0; k < C::BM / 16; ++k) {  // contraction over the 128 keys
-            mma_ss_w(t_s, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
-            if (has_gk) mma_ss_w(t_s, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
+          for (int u = 0; u < PER; ++u) sc[a * C::BN + lane + 32 * u] = -pre[a][u];
+        __syncwarp();
+        // the next tile's scalars are in flight while this warp waits below
+        if (t + 1 < T) fetch(q_next);
+        bool w = true;
+        if (lane == 0 && t >= C::STAGES)
+          w = wait_bar(qg_empty + s, ((t / C::STAGES) - 1) & 1, abort_st, prm.status);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) {
+          // this arrival publishes the scalars written above with the stage
+          mbar_arrive_expect_tx(qg_full + s, (has_gq ? 2 : 1) * C::QB);
+          load_pair_opt<D>(smem + C::OFF_QG + s * 2 * C::QB, &mQ, &mGQ, has_gq, qg_full + s,
+                           C::BN, q0, bh);
+          ++qg_issued;
+          if (t + 1 < T) {  // warm L2 with the next query tile
+            tma_prefetch_l2_4d(&mQ, 0, q_next, 0, bh);
+            if (has_gq) tma_prefetch_l2_4d(&mGQ, 0, q_next, 0, bh);
           }
-          mma_commit_w(gq_full);
-        };
-        // at d = 128 gradQ^T goes before gradV: its partial is drained sooner,
-        // and the next tile's scores wait for that drain
-        if (!C::SG2) issue_gq();
-#pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts_w(t_gv, t_g + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
-        mma_commit_w(do_empty + ds);
-        if (C::SG2) {
-          issue_gq();
-        } else if (t + 1 < T && !issue_sg(t + 1)) {
-          ok = false;
-          break;
         }
       }
-      if (ok) mma_commit_w(acc_done);
-      mma_commit_w(drain);
-      mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
+      // every load this warp issued has landed before the CTA exits (after an
+      // abort some were never awaited); each phase waited for is the last of
+      // its barrier, so on the normal path these return at once
+      if (lane == 0) {
+        mbar_wait_bounded(kv_full, 0, prm.status, 100000000ull);
+        for (int t = max(0, qg_issued - C::STAGES); t < qg_issued; ++t)
+          mbar_wait_bounded(qg_full + (t % C::STAGES), (t / C::STAGES) & 1, prm.status,
+                            100000000ull);
+      }
+    } else if (warp == kColDoWarp) {
+      if (lane == 0) {
+        int do_issued = 0;
+        for (int t = 0; t < T; ++t) {
+          const int ds = t % C::DSTAGES;
+          if (t >= C::DSTAGES &&
+              !wait_bar(do_empty + ds, ((t / C::DSTAGES) - 1) & 1, abort_st, prm.status))
+            break;
+          mbar_arrive_expect_tx(do_full + ds, C::QB);
+          load_tile(smem + C::OFF_DO + ds * C::QB, &mDO, do_full + ds,
+                    qstart + rotated(t, rot, T) * C::BN, bh);
+          ++do_issued;
+          if (t + 1 < T)  // warm L2 with the next dO tile
+            tma_prefetch_l2_4d(&mDO, 0, qstart + rotated(t + 1, rot, T) * C::BN, 0, bh);
+        }
+        // every load this thread issued has landed before the CTA exits
+        for (int t = max(0, do_issued - C::DSTAGES); t < do_issued; ++t)
+          mbar_wait_bounded(do_full + (t % C::DSTAGES), (t / C::DSTAGES) & 1, prm.status,
+                            100000000ull);
+      }
+    } else if (warp == kColMmaWarp) {
+      {  // the whole warp: warp-uniform waits, elect.sync issues each MMA
+        constexpr uint32_t id_sc = idesc_bf16(128, 64, false, false);  // scores: M=128 N=64
+        constexpr uint32_t id_sg = idesc_bf16(128, 128, false, false);  // K [Q;gQ]^T: N=128
+        constexpr uint32_t id_out = idesc_bf16(128, D, false, true);   // gradK/V: N=D, B MN
+        constexpr uint32_t id_gq = idesc_bf16(D, 64, true, true);      // gradQ^T: M=D, A,B MN
+        // descriptor low words of the stationary tiles: K-major for the score
+        // MMAs, MN-major (64-feature groups BM*128 bytes apart) for gradQ^T
+        const uint32_t k_lo = lo_kmajor(sb + C::OFF_K), gk_lo = lo_kmajor(sb + C::OFF_GK),
+                       v_lo = lo_kmajor(sb + C::OFF_V), gv_lo = lo_kmajor(sb + C::OFF_GV);
+        const uint32_t k_mn = lo_mnmajor(sb + C::OFF_K, C::BM * 128),
+                       gk_mn = lo_mnmajor(sb + C::OFF_GK, C::BM * 128);
+        const uint32_t ds_mn = lo_mnmajor(sb + C::OFF_DS, 1024), gs_mn = lo_mnmajor(sb + C::OFF_GS, 1024);
+        const uint32_t t_dp = tmem + C::T_DP, t_h = tmem + C::T_H, t_gk = tmem + C::T_GK,
+                       t_gv = tmem + C::T_GV;
+        // dP^T and H^T of tile t (need dO(t) and the previous tile's scores
+        // read out of TMEM)
+        auto issue_dh = [&](int t) -> bool {
+          const int ds = t % C::DSTAGES;
+          const uint32_t do_lo = opaque(lo_kmajor(sb + C::OFF_DO + ds * C::QB));
+          const uint32_t v_l = opaque(v_lo), gv_l = opaque(gv_lo);
+          if (!warp_wait(do_full + ds, (t / C::DSTAGES) & 1, abort_st, prm.status)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss_w(t_dp, v_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc, k > 0 ? 1u : 0u);
+          if (has_gv) {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              mma_ss_w(t_h, gv_l + kslice_off(C::BM, k), do_lo + kslice_off(C::BN, k), id_sc,
+                     k > 0 ? 1u : 0u);
+          }
+          return true;
+        };
+        // S^T and G^T of tile t into buffer t % 2 (need Q, gQ; overwrite the
+        // A operands and the gradQ^T partial of the tile that last used the
+        // buffer: t - 1 at d = 128, t - 2 with SG2), then the commit that
+        // covers all four score blocks
+        auto issue_sg = [&](int t) -> bool {
+          const int s = t % C::STAGES;
+          const uint32_t qgq_lo = opaque(lo_kmajor(sb + C::OFF_QG + s * 2 * C::QB));  // [Q;gQ] per half
+          const uint32_t k_l = opaque(k_lo), gk_l = opaque(gk_lo);
+          const uint32_t t_s = tmem + C::T_S(t & 1), t_g = tmem + C::T_G(t & 1);
+          const int prev = C::SG2 ? t - 2 : t - 1;  // the buffer's previous tile
+          if (!warp_wait(qg_full + s, (t / C::STAGES) & 1, abort_st, prm.status)) return false;
+          if (prev >= 0 && !warp_wait(gq_empty, prev & 1, abort_st, prm.status)) return false;
+          tc_fence_after();
+          // [S^T | K gQ^T] = K [Q; gQ]^T (S^T = K Q^T alone without gQ), then
+          // G^T += gK Q^T (the first BN rows of each [Q;gQ] half are Q)
+          const uint32_t id_first = has_gq ? id_sg : id_sc;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss_w(t_s, k_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_first,
+                   k > 0 ? 1u : 0u);
+          if (has_gk) {
+            const uint32_t g0 = has_gq ? 1u : 0u;  // without gQ this starts G^T
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              mma_ss_w(t_g, gk_l + kslice_off(C::BM, k), qgq_lo + kslice_off(2 * C::BN, k), id_sc,
+                     k > 0 ? 1u : g0);
+          }
+          mma_commit_w(sc_full);
+          return true;
+        };
+        bool ok = warp_wait(kv_full, 0, abort_st, prm.status) && issue_dh(0) && issue_sg(0);
+        for (int t = 0; ok && t < T; ++t) {
+          const int s = t % C::STAGES, ds = t % C::DSTAGES;
+          // ---- next tile's dP^T, H^T while the elementwise warps work ----
+          if (t + 1 < T) {
+            if (!warp_wait(sc_read, t & 1, abort_st, prm.status)) { ok = false; break; }
+            tc_fence_after();
+            if (!issue_dh(t + 1)) { ok = false; break; }
+          }
+          // ---- SG2: next tile's S^T, G^T into the other buffer ----
+          if (C::SG2 && t + 1 < T && !issue_sg(t + 1)) { ok = false; break; }
+          // ---- outputs: A operands (bf16 gS^T, dS^T, gdP^T) from TMEM ----
+          if (!warp_wait(ds_full, t & 1, abort_st, prm.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t t_s = tmem + C::T_S(t & 1), t_g = tmem + C::T_G(t & 1);
+          const uint32_t qgq_s = sb + C::OFF_QG + s * 2 * C::QB;
+          // B operands MN-major: 64-feature groups 2*BN*128 bytes apart in the
+          // interleaved [Q;gQ] stage, BN*128 apart in the dO tile
+          const uint32_t q_mn = opaque(lo_mnmajor(qgq_s, 2 * C::BN * 128)),
+                         gq_mn = opaque(lo_mnmajor(qgq_s + C::BN * 128, 2 * C::BN * 128));
+          const uint32_t do_mn = opaque(lo_mnmajor(sb + C::OFF_DO + ds * C::QB, C::BN * 128));
+          const uint32_t first = t > 0 ? 1u : 0u;
+          // gradK first: it releases the [Q|gQ] stage that the next tile waits for
+#pragma unroll
+          for (int k = 0; k < C::BN / 16; ++k) {  // contraction over the 64 queries
+            mma_ts_w(t_gk, t_s + 16 * k, q_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+            if (has_gq) mma_ts_w(t_gk, t_s + 16 * k + 8, gq_mn + kstep_off(k), id_out, 1u);
+          }
+          mma_commit_w(qg_empty + s);
+          // gradQ^T of tile t into its S^T columns, whose A operands the gradK
+          // MMAs above read first (MMAs from one thread run in issue order).
+          // The partial that used them before was drained before this tile's
+          // S^T / G^T were issued.
+          auto issue_gq = [&]() {
+            const uint32_t k_m = opaque(k_mn), gk_m = opaque(gk_mn), ds_m = opaque(ds_mn),
+                           gs_m = opaque(gs_mn);
+#pragma unroll
+            for (int k = 0; k < C::BM / 16; ++k) {  // contraction over the 128 keys
+              mma_ss_w(t_s, k_m + kstep_off(k), gs_m + kstep_off(k), id_gq, k > 0 ? 1u : 0u);
+              if (has_gk) mma_ss_w(t_s, gk_m + kstep_off(k), ds_m + kstep_off(k), id_gq, 1u);
+            }
+            mma_commit_w(gq_full);
+          };
+          // at d = 128 gradQ^T goes before gradV: its partial is drained sooner,
+          // and the next tile's scores wait for that drain
+          if (!C::SG2) issue_gq();
+#pragma unroll
+          for (int k = 0; k < C::BN / 16; ++k)
+            mma_ts_w(t_gv, t_g + 16 * k, do_mn + kstep_off(k), id_out, k > 0 ? 1u : first);
+          mma_commit_w(do_empty + ds);
+          if (C::SG2) {
+            issue_gq();
+          } else if (t + 1 < T && !issue_sg(t + 1)) {
+            ok = false;
+            break;
+          }
+        }
+        if (ok) mma_commit_w(acc_done);
+        mma_commit_w(drain);
+        mbar_wait_bounded(drain, 0, prm.status, 100000000ull);
+      }
     }
   } else {
+    regs_claim<C::REGS_ELEMENTWISE>();
     // ---------------- elementwise warps: thread = key row -----------------
     constexpr int NC = kColCols;           // query columns per thread
     const int row = 32 * (warp & 3) + lane;
@@ -1101,6 +1120,20 @@ __global__ void __launch_bounds__(256) gradq_convert(const float4* __restrict__ 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+// Whether the pass-2 kernel's launch registers (per thread, as compiled)
+// cover the warpgroup split it performs; looked up once per instantiation.
+template <int D>
+bool col_regs_cover_split(bool all) {
+  auto covers = [](const void* fn) {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, fn) == cudaSuccess &&
+           (long long)fa.numRegs * kColThreads >= Col<D>::REGS_NEEDED;
+  };
+  static const bool ok_all = covers(reinterpret_cast<const void*>(bob_col_pass<D, true>));
+  static const bool ok_some = covers(reinterpret_cast<const void*>(bob_col_pass<D, false>));
+  return all ? ok_all : ok_some;
+}
+
 template <int D>
 cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v, const void* o,
                   const float* lse, const void* dO, const void* gq, const void* gk,
@@ -1126,6 +1159,9 @@ cudaError_t bob_d(const Problem& p, const void* q, const void* k, const void* v,
   const bool all = has_gq && has_gk && has_gv;
   auto row_kernel = all ? bob_row_pass<D, true> : bob_row_pass<D, false>;
   auto col_kernel = all ? bob_col_pass<D, true> : bob_col_pass<D, false>;
+  // pass 2 moves registers between its warpgroups; refuse to launch a build
+  // whose register count cannot cover that split (the claim would not end)
+  if (!col_regs_cover_split<D>(all)) return cudaErrorLaunchOutOfResources;
   cudaError_t e = cudaFuncSetAttribute(row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)R::SMEM);
   if (e != cudaSuccess) return e;
