@@ -395,8 +395,6 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
-// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32); inputs are
-// scores minus the row log-sum-exp, so results lie in [0, 1] up to rounding.
 // Warpgroup register reallocation (PTX ISA: setmaxnreg).  Every thread of
 // a warpgroup (four consecutive warps) must execute the same instruction.
 // A release returns registers to the CTA's pool; a claim waits until the
@@ -413,6 +411,8 @@ __device__ __forceinline__ void regs_claim() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
 }
 
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32); inputs are
+// scores minus the row log-sum-exp, so results lie in [0, 1] up to rounding.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -32,7 +32,9 @@
 // per CTA: elementwise warps (thread = TMEM lane), TMA producer warps (one
 // issuing thread each), a warp that allocates TMEM and issues tcgen05.mma
 // with all its lanes (elect.sync picks the issuing lane), and in pass 1 a
-// helper warp that folds the MMA warp's waits.  Every wait is bounded (see
+// helper warp that folds the MMA warp's waits.  In pass 2 the control warps
+// form one warpgroup (with an idle fourth warp) that hands registers to the
+// elementwise warpgroups (setmaxnreg).  Every wait is bounded (see
 // common.cuh).
 #include <cuda.h>
 #include <cuda_bf16.h>
