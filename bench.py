@@ -100,9 +100,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or
-    None if there is none or the kernel sources changed since the capture."""
+def recorded_counters(kernel: str, workload: str):
+    """The committed ncu record of `kernel` on `workload`
+    (profiles/dram_traffic.json), or None if there is none or the kernel
+    sources changed since the capture."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
@@ -111,7 +112,25 @@ def recorded_traffic(kernel: str, workload: str):
     entry = rec.get(workload, {}).get(kernel)
     if not entry or entry.get("source_hash") != kernel_source_hash():
         return None
-    return entry.get("bytes_per_launch")
+    return entry
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu record."""
+    entry = recorded_counters(kernel, workload)
+    return entry.get("bytes_per_launch") if entry else None
+
+
+def recorded_smem(kernel: str, workload: str):
+    """Busy fraction of the SM's shared-memory data pipe during `kernel`
+    (tensor-core operand reads and LSU accesses, each per cycle against one
+    wavefront per cycle), from the committed ncu record; None without one."""
+    entry = recorded_counters(kernel, workload)
+    if not entry or "smem_tc_pct" not in entry or "smem_lsu_pct" not in entry:
+        return None
+    tc, lsu = entry["smem_tc_pct"] / 100.0, entry["smem_lsu_pct"] / 100.0
+    return {"tensor_core": tc, "lsu": lsu, "total": tc + lsu,
+            "source": "ncu l1tex__data_pipe_{tc,lsu}_wavefronts_mem_shared"}
 
 
 class ClockSampler:
@@ -352,7 +371,8 @@ def run_ours(args, w, rank, world, dist):
                      "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_kind": f"bf16 dense burst ({peaks.get('source')})",
                      "frac_of_sustained": achieved / sustained,
-                     "traffic": recorded_traffic(dom[0], w.name)},
+                     "traffic": recorded_traffic(dom[0], w.name),
+                     "smem_busy": recorded_smem(dom[0], w.name)},
         "peak_mem_gib": peak_mem / 2**30,
         "cpu_baseline": cpu,
         "e2e": e2e,

@@ -51,3 +51,21 @@ def test_warmup_below_three_is_refused():
     out = subprocess.run([sys.executable, "bench.py", "--warmup", "2"], cwd=ROOT,
                          capture_output=True, text=True, timeout=120)
     assert out.returncode != 0
+
+
+def test_recorded_counters_follow_the_kernel_sources(tmp_path, monkeypatch):
+    """The ncu figures in the JSON line (DRAM traffic, shared-memory busy
+    fraction) are reported only while the kernel sources still hash to the
+    value recorded with the capture."""
+    rec = {"wl": {"k": {"bytes_per_launch": 123.0, "smem_tc_pct": 57.0, "smem_lsu_pct": 20.0,
+                        "source_hash": "abc"}}}
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc")
+    assert bench.recorded_traffic("k", "wl") == 123.0
+    smem = bench.recorded_smem("k", "wl")
+    assert abs(smem["total"] - 0.77) < 1e-12 and abs(smem["tensor_core"] - 0.57) < 1e-12
+    assert bench.recorded_smem("other", "wl") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "changed")
+    assert bench.recorded_traffic("k", "wl") is None and bench.recorded_smem("k", "wl") is None
