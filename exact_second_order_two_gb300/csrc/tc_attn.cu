@@ -17,7 +17,8 @@
 //   columns as the A operands of dV += P^T dO and dK += dS^T Q; the next
 //   tile's scores are issued before this tile's dQ^T = K^T dS^T, which the
 //   elementwise warps read out one tile late and stage in shared memory; a
-//   TMA reduce-add carries it into an fp32 accumulator, then converted.
+//   TMA reduce-add carries it into an fp32 accumulator (at d = 128 half of
+//   the features, the other half by red.global), then converted.
 //
 // Warp roles as in the BoB kernels: elementwise warps own TMEM lanes, one TMA
 // producer warp, one MMA warp (TMEM allocator; elect.sync picks the issuing
@@ -437,11 +438,16 @@ struct Bwd {
   static constexpr uint32_t OFF_DS = OFF_DO + DSTAGES * QB;
   static constexpr uint32_t OFF_SC = OFF_DS + XB;            // [STAGES][2][BN] fp32
   // dQ^T partials go from TMEM to global memory through shared memory: the
-  // elementwise warps write a tile's partial as [BN][D] fp32 rows into a
-  // staging buffer and a TMA reduce-add carries it into the accumulator
-  // (one buffer at d = 128, two at d = 64)
-  static constexpr uint32_t STGB = BN * D * 4;
-  static constexpr int SBUF = D == 64 ? 2 : 1;
+  // elementwise warps write a tile's partial as [BN][SF] fp32 rows into one
+  // of two staging buffers and a TMA reduce-add carries it into the
+  // accumulator.  At d = 128 the staging carries features 0-63 only; the
+  // threads holding features 64-127 add theirs with red.global.  Shared
+  // memory is this kernel's limit (MMA operand reads, the dS^T stores and
+  // the staging round trip), and halving the staged bytes took the
+  // benchmark workload's first backward from 4.70 to 4.51 ms.
+  static constexpr int SF = D == 128 ? 64 : D;  // features staged per row
+  static constexpr uint32_t STGB = BN * SF * 4;
+  static constexpr int SBUF = 2;
   static constexpr uint32_t OFF_STG = (OFF_SC + STAGES * 2 * BN * 4 + 1023) / 1024 * 1024;
   static constexpr uint32_t OFF_MISC = OFF_STG + SBUF * STGB;
   static constexpr uint32_t MISC = 512;
@@ -471,11 +477,13 @@ struct BwdParams {
   int N, causal;
   int BH, G;  // batch * heads, heads per CTA group (cta_coord)
   float scale;
+  float* acc;  // fp32 dQ accumulator, for the features the staging does not carry
 };
 
 // Warps 0-15 elementwise, 16 TMA producer, 17 MMA issuer, 18 issues the TMA
-// reduce-add of each staged dQ^T partial (per-thread atomics for them kept
-// the elementwise warps issuing for over a thousand cycles per tile).
+// reduce-add of each staged dQ^T partial (per-thread atomics for the whole
+// partial kept the elementwise warps issuing for over a thousand cycles per
+// tile; at d = 128 they carry half of it, which relieves shared memory).
 constexpr int kBwdConsumerWarps = 16;
 constexpr int kBwdConsumers = kBwdConsumerWarps * 32;
 constexpr int kBwdProducerWarp = kBwdConsumerWarps;
@@ -753,10 +761,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(dq_empty);
       return true;
     };
-    // dQ^T partial of tile u into staging buffer u % SBUF as [BN][D] fp32
-    // rows (query column c, feature f at c * D + f; a warp's lanes write
+    // dQ^T partial of tile u into staging buffer u % SBUF as [BN][SF] fp32
+    // rows (query column c, feature f at c * SF + f; a warp's lanes write
     // consecutive words) once the reduce-add that last used the buffer has
-    // read it, then the arrival that hands it to the reduce warp
+    // read it, then the arrival that hands it to the reduce warp.  Features
+    // from SF on (d = 128) go to the accumulator directly.
     auto stage_dq = [&](int u, const uint32_t (&dq)[NC]) -> bool {
       const int b = u % C::SBUF;
       if (u >= C::SBUF &&
@@ -765,10 +774,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // M = 64 accumulator at d = 64: rows 16w' + x (w' = warp & 3, x < 16)
       // live in lanes 32w' + x; the upper 16 lanes of each warp hold nothing
       const int f = D == 128 ? row : 16 * (warp & 3) + lane;
-      if (D == 128 || lane < 16) {
-        const uint32_t base = sb + C::OFF_STG + b * C::STGB + (uint32_t)(NC * slice * D + f) * 4u;
+      if (D == 128 && f >= C::SF) {
+        const int qa = qstart + rotated(u, rot, T) * C::BN + NC * slice;
+        red_columns<D, NC>(prm.acc + ((size_t)bh * N + qa) * D + f, dq, N - qa);
+      } else if (D == 128 || lane < 16) {
+        const uint32_t base = sb + C::OFF_STG + b * C::STGB + (uint32_t)(NC * slice * C::SF + f) * 4u;
 #pragma unroll
-        for (int i = 0; i < NC; ++i) st_shared_u32(base + (uint32_t)(i * D * 4), dq[i]);
+        for (int i = 0; i < NC; ++i) st_shared_u32(base + (uint32_t)(i * C::SF * 4), dq[i]);
       }
       fence_async_smem();
       mbar_arrive(stg_full + b);
@@ -964,11 +976,12 @@ cudaError_t backward_d(const Problem& p, const void* q, const void* k, const voi
       !make_map(&mQ, q, p, C::BN) || !make_map(&mDO, dO, p, C::BN))
     return cudaErrorInvalidValue;
   CUtensorMap mAcc;
-  if (!make_acc_map(&mAcc, ws.acc, p, C::BN)) return cudaErrorInvalidValue;
+  if (!make_acc_map(&mAcc, ws.acc, p, C::SF, C::BN)) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(bwd_col_pass<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::SMEM);
   if (e != cudaSuccess) return e;
   BwdParams bp;
+  bp.acc = ws.acc;
   bp.lse = lse;
   bp.Dv = ws.D;
   bp.dk = static_cast<__nv_bfloat16*>(dk);

@@ -191,14 +191,16 @@ inline bool make_map(CUtensorMap* m, const void* ptr, const Problem& p, int box_
 }
 
 // [B*H, N, D] fp32 accumulator viewed 3-D as (D features, N rows, B*H
-// heads); one box = box_rows rows x all D features, [box_rows][D] fp32 rows
-// in shared memory without swizzle.  A reduce-add skips rows past N.
-inline bool make_acc_map(CUtensorMap* m, float* ptr, const Problem& p, int box_rows) {
+// heads); one box = box_rows rows x the first box_cols features,
+// [box_rows][box_cols] fp32 rows in shared memory without swizzle.  A
+// reduce-add skips rows past N.
+inline bool make_acc_map(CUtensorMap* m, float* ptr, const Problem& p, int box_cols,
+                         int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.N, (cuuint64_t)p.BH()};
   cuuint64_t strides[2] = {(cuuint64_t)p.d * 4, (cuuint64_t)p.N * p.d * 4};
-  cuuint32_t box[3] = {(cuuint32_t)p.d, (cuuint32_t)box_rows, 1};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
