@@ -11,7 +11,10 @@
 //   P = 2^(S c log2 e - m) is written over it and O += P V accumulates in
 //   TMEM.  The reference maximum m moves only when a tile's maximum exceeds
 //   it by more than 8 (log2 units), and O is then rescaled in TMEM; the
-//   epilogue divides by the row sum and writes LSE.
+//   epilogue divides by the row sum and writes LSE.  At d = 128 the four
+//   column slices of a row share m (agreed per tile through shared memory);
+//   at d = 64 each slice has its own m and its own O, combined in the
+//   epilogue.
 // first backward (key-stationary, 128 key rows per CTA, 64-query tiles):
 //   S^T and dP^T into TMEM; bf16 P^T and dS^T written back into the S^T
 //   columns as the A operands of dV += P^T dO and dK += dS^T Q; the next
@@ -74,7 +77,8 @@ struct Fwd {
   static constexpr uint32_t SMEM = OFF_MISC + MISC;
   static_assert(SMEM <= 232448, "forward shared memory budget");
   // TMEM columns: S (two buffers of 128), O, bf16 Q as the A operand of
-  // S = Q K^T.  Each elementwise thread writes bf16 P over the first 16 of
+  // S = Q K^T (at d = 64: four O's, one per slice, and Q stays in shared
+  // memory).  Each elementwise thread writes bf16 P over the first 16 of
   // the 32 S columns it read: keys 32s + 2c, + 1 of slice s in column
   // 32s + c, so 16-key step k of P V sits at p_col(k).
   static constexpr uint32_t T_O = 256, TMEM_COLS = 512;
@@ -86,6 +90,14 @@ struct Fwd {
   // exceeds it by more than kRescale: P = 2^(S c log2 e - m) then stays
   // below 2^kRescale, and O is rescaled in TMEM only on those rare moves.
   static constexpr float kRescale = 8.f;
+  // d = 64: one O accumulator per column slice (columns 256 + 64 s), each
+  // with its own reference maximum, combined in the epilogue.  At d = 64 the
+  // tile's MMAs (about 640 cycles) do not hide a per-tile exchange of the
+  // row maximum between the slices; without it the forward at 4 x 262144
+  // went from 45.3 to 42.8 ms.  S = Q K^T then takes Q from shared memory:
+  // the TMEM columns of its copy hold the fourth O, and an N=128 MMA costs
+  // the same with both operands in shared memory.
+  static constexpr bool PSO = D == 64;
 };
 
 struct FwdParams {
@@ -233,8 +245,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t v_mn = opaque(lo_mnmajor(sb + C::OFF_V + vs * C::KB, C::BN * 128));
         const uint32_t t_p = tmem + C::T_S(pb);
 #pragma unroll
-        for (int k = 0; k < C::BN / 16; ++k)
-          mma_ts_w(t_o, t_p + C::p_col(k), v_mn + kstep_off(k), id_o, (t > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < C::BN / 16; ++k) {
+          // PSO: key steps 2s, 2s + 1 are slice s's, into its own O
+          const uint32_t to = C::PSO ? t_o + 64u * (uint32_t)(k >> 1) : t_o;
+          const bool chained = C::PSO ? (k & 1) != 0 : k > 0;
+          mma_ts_w(to, t_p + C::p_col(k), v_mn + kstep_off(k), id_o, (t > 0 || chained) ? 1u : 0u);
+        }
         mma_commit_w(v_empty + vs);
         mma_commit_w(o_ready);
         return true;
@@ -247,10 +263,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (t >= 2 && !warp_wait(s_empty + b, ((t >> 1) - 1) & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_lo = opaque(lo_kmajor(sb + C::OFF_K + s * C::KB));
+        const uint32_t q_lo = opaque(lo_kmajor(sb + C::OFF_Q));
         const uint32_t t_s = tmem + C::T_S(b);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ts_w(t_s, t_q + 8 * k, k_lo + kslice_off(C::BN, k), id_s, k > 0 ? 1u : 0u);
+        for (int k = 0; k < D / 16; ++k) {
+          if (C::PSO)
+            mma_ss_w(t_s, q_lo + kslice_off(C::BM, k), k_lo + kslice_off(C::BN, k), id_s,
+                     k > 0 ? 1u : 0u);
+          else
+            mma_ts_w(t_s, t_q + 8 * k, k_lo + kslice_off(C::BN, k), id_s, k > 0 ? 1u : 0u);
+        }
         mma_commit_w(s_full + b);
         mma_commit_w(k_empty + s);
         if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
@@ -275,7 +297,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (ok) {
       // stationary Q row -> TMEM (bf16 pairs, lower half = even feature): one
       // 64-feature half-row per thread of slices 0 .. D/64 - 1
-      if (slice < D / 64) {
+      if (!C::PSO && slice < D / 64) {
         const uint32_t src = C::OFF_Q + slice * C::BM * 128 + row * 128;
         uint32_t lo[16], hi[16];
 #pragma unroll
@@ -324,13 +346,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // wait on an mbarrier (one buffer per tile parity: a buffer is
       // rewritten only after every thread has arrived for the next tile,
       // hence after it read this one)
-      float* rt = red + b * NS * 128;
-      rt[slice * 128 + row] = mx * sc2;
-      mbar_arrive(red_full + b);
-      if (!warp_wait(red_full + b, (t >> 1) & 1, abort_st, prm.status)) { ok = false; break; }
-      float mt = -INFINITY;
+      float mt = mx * sc2;  // PSO: this slice's own maximum is its reference
+      if (!C::PSO) {
+        float* rt = red + b * NS * 128;
+        rt[slice * 128 + row] = mt;
+        mbar_arrive(red_full + b);
+        if (!warp_wait(red_full + b, (t >> 1) & 1, abort_st, prm.status)) { ok = false; break; }
+        mt = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < NS; ++u) mt = fmaxf(mt, rt[u * 128 + row]);
+        for (int u = 0; u < NS; ++u) mt = fmaxf(mt, rt[u * 128 + row]);
+      }
       // the reference maximum moves (the same decision in every slice of a
       // row; rows, i.e. lanes, decide independently)
       const bool move = mt > m + C::kRescale;
@@ -345,7 +370,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!warp_wait(o_ready, (t - 1) & 1, abort_st, prm.status)) { ok = false; break; }
         tc_fence_after();
         const float f = scale_o ? alpha : 1.f;
-        constexpr int PART = D / NS;
+        constexpr int PART = C::PSO ? D : D / NS;  // PSO: the slice's whole O
 #pragma unroll
         for (int cc = 0; cc < PART; cc += 16) {
           uint32_t v[16];
@@ -384,10 +409,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // gets to this barrier, also after a failed wait
     float* part = red + 2 * NS * 128;
     part[slice * 128 + row] = l;
+    if (C::PSO) red[slice * 128 + row] = m;
     named_sync<kFwdConsumers>(1);
     float L = 0.f;
+    float fs[NS];  // PSO: weight of slice u's O and sum against the row maximum
+    if (C::PSO) {
+      float M = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < NS; ++u) L += part[u * 128 + row];
+      for (int u = 0; u < NS; ++u) M = fmaxf(M, red[u * 128 + row]);
+#pragma unroll
+      for (int u = 0; u < NS; ++u) {
+        const float mu = red[u * 128 + row];
+        fs[u] = mu > -INFINITY ? ex2_approx(mu - M) : 0.f;
+        L += part[u * 128 + row] * fs[u];
+      }
+      m = M;
+    } else {
+#pragma unroll
+      for (int u = 0; u < NS; ++u) L += part[u * 128 + row];
+    }
     ok = __all_sync(0xffffffffu, ok);
     if (ok) ok = warp_wait(o_ready, (T - 1) & 1, abort_st, prm.status);
     tc_fence_after();
@@ -398,7 +438,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < PART; cc += 16) {
         uint32_t v[16];
-        tmem_ld16(tmem + lane_off + C::T_O + PART * slice + cc, v);
+        if (C::PSO) {
+          float a[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) a[e] = 0.f;
+#pragma unroll
+          for (int u = 0; u < NS; ++u) {
+            tmem_ld16(tmem + lane_off + C::T_O + 64u * u + PART * slice + cc, v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) a[e] = fmaf(fs[u], __uint_as_float(v[e]), a[e]);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(a[e]);
+        } else {
+          tmem_ld16(tmem + lane_off + C::T_O + PART * slice + cc, v);
+        }
         if (row_ok) {
 #pragma unroll
           for (int q = 0; q < 2; ++q)
